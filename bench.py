@@ -1,0 +1,429 @@
+"""Throughput of the tile-signalled MoE expert-combine path on GB300.
+
+One step = the whole path over one batch of synthetic input: gate routing,
+plan build (layout, schedule, combine plan) with the layout gather, the
+overlapped expert FFN producer and combine consumer, and the scale. The
+workload is the 4-rank A100-paper-like layer (W=4, 2 experts/rank, top-2,
+4096 tokens/rank, d_model 2048, d_ff 8192, tb_M 128, balanced routing).
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle on the
+host cores instead (a bounded sample of the same workload).
+Multi-GPU: the path does not shard across GPUs (all logical ranks live on one
+GPU), so `--gpus N` runs N independent replicas, one per GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "a100_like"
+METRIC = "MoE combine-layer tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == 7:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+
+    from tile_signaled_grouped_gb300 import capi
+    from tile_signaled_grouped_gb300.runtime import ExpertCombine
+    from tile_signaled_grouped_gb300.workloads import get_workload, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    wl = get_workload(args.workload)
+    W, T, D, F, k = wl.W, wl.T, wl.d_model, wl.d_ff, wl.topk
+    inp = make_inputs(wl, device="cuda")
+    layer = ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas)
+    sp = torch.cuda.Stream()
+    sc = torch.cuda.Stream(priority=-1)
+
+    def step():
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                      producer=sp, consumer=sc)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, detail = layer.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail}")
+
+    # Counts for the algorithmic work of one step (read once, outside the timed region).
+    rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
+    recv_rows = layer.field(capi.MOE_PLAN_RECV_ROWS).cpu().tolist()
+    rows_exec = sum(rank_rows)
+    valid_rows = W * T * k
+    flops_exec = 6.0 * rows_exec * D * F
+    flops_valid = 6.0 * valid_rows * D * F
+
+    # ---- timed region: K steps, inputs resident in HBM ------------------------------
+    layer.set_timing(True)
+    prod_ms, cons_ms = [], []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        ev0.record(sp)
+        for _ in range(args.steps):
+            step()
+            t = layer.timings()  # waits for this step's events (one step in flight)
+            prod_ms.append(t[2])
+            cons_ms.append(t[3])
+        ev1.record(sp)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    layer.set_timing(False)
+
+    # The per-step event read above serialises steps on the host; time the same K steps
+    # again back to back without reading timings, and take that as the step time.
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ev0.record(sp)
+    for _ in range(args.steps):
+        step()
+    ev1.record(sp)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_free = ev0.elapsed_time(ev1)
+    ms_step = ms_free / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    code, detail = layer.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail} after the timed region")
+
+    # ---- stage measurements (outside the timed region) --------------------------------
+    stages = stage_times(layer, inp, wl, sp, sc, args)
+
+    # ---- e2e through the C ABI with host buffers ----------------------------------------
+    e2e = e2e_arm(layer, inp, wl, sp, sc, args)
+
+    hbm, bf16, bf16_sus, src = _peaks()
+    prod_avg = statistics.mean(prod_ms)
+    achieved = flops_exec / (prod_avg * 1e-3) / 1e12
+    result = {
+        "metric": METRIC,
+        "value": world * W * T / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: x~N(0,1), weights~N(0,0.02), logits~N(0,1), balanced routing)",
+        "config": {"workload": wl.name, "W": W, "experts_per_rank": wl.L, "topk": k,
+                   "tokens_per_rank": T, "d_model": D, "d_ff": F, "tb_M": wl.tb_M,
+                   "mgb": wl.mgb, "consumer_ctas": args.consumer_ctas,
+                   "parallelism": f"{W} logical EP ranks on 1 GPU; replicas x{world}",
+                   "l2": "inputs larger than L2: 768 MB of expert weights read every step"},
+        "roofline": {"kernel": "ffn_producer (GEMM1+SiLU+GEMM2, executed rows)",
+                     "bound": "tensor", "achieved": achieved, "peak": bf16_sus,
+                     "unit": "TFLOP/s", "frac": achieved / bf16_sus, "traffic": None,
+                     "peak_source": f"{src} bf16 sustained (kernel timed inside a loop of steps)",
+                     "flops_per_launch": flops_exec, "launch_ms": prod_avg},
+        "e2e": e2e,
+        "gpu_launches": 10 * args.steps,
+        "clocks": clk.summary(),
+        "stages": stages,
+        "work": {"rows_executed": rows_exec, "rows_valid": valid_rows,
+                 "tflop_executed": flops_exec / 1e12, "tflop_valid": flops_valid / 1e12,
+                 "recv_rows": recv_rows},
+        "timed_wall_s": wall,
+        "timed_event_ms": ms_total,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    layer.close()
+    return result
+
+
+def stage_times(layer, inp, wl, sp, sc, args, iters=5):
+    """Per-kernel times of one step, and the producer alone on every SM (serial mode)."""
+    import torch
+
+    from tile_signaled_grouped_gb300 import capi
+
+    W, T, D, k = wl.W, wl.T, wl.d_model, wl.topk
+    hbm, bf16, bf16_sus, _ = _peaks()
+    layer.set_timing(True)
+    acc = {}
+    for _ in range(iters):
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                      producer=sp, consumer=sc)
+        t = layer.timings()
+        for i, name in enumerate(["route", "plan", "producer", "consumer", "scale", "gather"]):
+            acc.setdefault(name, []).append(t[i])
+    over = {n: statistics.median(v) for n, v in acc.items()}
+    # serial mode: the producer on all SMs, then the consumer on all SMs with every flag set
+    ser = {}
+    serial = capi.moe_cfg(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, 0, 0)
+    from tile_signaled_grouped_gb300.runtime import ExpertCombine
+    lay2 = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, 0)
+    lay2.set_timing(True)
+    for _ in range(iters):
+        lay2.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                     producer=sp)
+        t = lay2.timings()
+        for i, name in enumerate(["route", "plan", "producer", "consumer", "scale", "gather"]):
+            ser.setdefault(name, []).append(t[i])
+    ser = {n: statistics.median(v) for n, v in ser.items()}
+    del serial
+    rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
+    recv_rows = layer.field(capi.MOE_PLAN_RECV_ROWS).cpu().tolist()
+    rows = sum(rank_rows)
+    valid = W * T * k
+    flops = 6.0 * rows * D * wl.d_ff
+    cons_bytes = 4.0 * D * sum(recv_rows)
+    scale_bytes = 2.0 * D * k * W * T + 2.0 * D * W * T + 8.0 * W * T * k
+    gather_bytes = 2.0 * D * (valid + rows)
+    lay2.close()
+    return {
+        "overlapped_ms": over,
+        "serial_ms": ser,
+        "producer_alone_tflops": flops / (ser["producer"] * 1e-3) / 1e12,
+        "producer_alone_frac_burst": flops / (ser["producer"] * 1e-3) / 1e12 / bf16,
+        "producer_overlapped_tflops": flops / (over["producer"] * 1e-3) / 1e12,
+        "overlap_vs_gemm_alone": max(over["producer"], over["consumer"]) / ser["producer"],
+        "consumer_standalone_gbs": cons_bytes / (ser["consumer"] * 1e-3) / 1e9,
+        "consumer_standalone_frac": cons_bytes / (ser["consumer"] * 1e-3) / 1e9 / hbm,
+        "scale_gbs": scale_bytes / (over["scale"] * 1e-3) / 1e9,
+        "scale_frac": scale_bytes / (over["scale"] * 1e-3) / 1e9 / hbm,
+        "gather_gbs": gather_bytes / (over["gather"] * 1e-3) / 1e9,
+        "gather_frac": gather_bytes / (over["gather"] * 1e-3) / 1e9 / hbm,
+    }
+
+
+def e2e_arm(layer, inp, wl, sp, sc, args):
+    """Same metric through the C ABI with pinned host buffers: inputs copied in and
+    the output copied out inside the timed region, every step."""
+    import torch
+
+    W, T, D = wl.W, wl.T, wl.d_model
+    hx = [t.cpu().pin_memory() for t in inp.x]
+    hl = inp.logits.cpu().pin_memory()
+    hf = None if inp.forced_ids is None else inp.forced_ids.cpu().pin_memory()
+    dx = [torch.empty_like(t) for t in inp.x]
+    dl = torch.empty_like(inp.logits)
+    df = None if hf is None else torch.empty_like(inp.forced_ids)
+    hout = [torch.empty(T, D, dtype=torch.bfloat16).pin_memory() for _ in range(W)]
+    h2d = sum(t.numel() * t.element_size() for t in hx) + hl.numel() * 4 + \
+        (0 if hf is None else hf.numel() * 4)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def step():
+        with torch.cuda.stream(sp):
+            for d, h in zip(dx, hx):
+                d.copy_(h, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            if df is not None:
+                df.copy_(hf, non_blocking=True)
+        layer.forward(dx, inp.w_gate, inp.w_up, inp.w_down, dl, df, producer=sp, consumer=sc)
+        with torch.cuda.stream(sp):
+            for h, o in zip(hout, layer.out):
+                h.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, args.steps)
+    ev0.record(sp)
+    for _ in range(n):
+        step()
+    ev1.record(sp)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / n
+    return {"value": W * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(wl, seconds=15.0, max_tokens=None):
+    """The oracle, as it stands, on the host cores: route, plan, FFN, combine and scale
+    of the same workload with the first n tokens of every rank (n sized to run for
+    about `seconds`). Returns tokens/s."""
+    import numpy as np
+
+    from oracle import moe_oracle as O
+    from tile_signaled_grouped_gb300.workloads import make_inputs
+
+    inp = make_inputs(wl, device="cpu")
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    xs = [f64(t) for t in inp.x]
+    wg = [f64(t) for t in inp.w_gate]
+    wu = [f64(t) for t in inp.w_up]
+    wd = [f64(t) for t in inp.w_down]
+    lg = inp.logits.numpy()
+    forced = None if inp.forced_ids is None else inp.forced_ids.numpy()
+
+    def run(n):
+        t0 = time.perf_counter()
+        O.forward([x[:n] for x in xs], wg, wu, wd, lg[:, :n], wl.topk, wl.L, wl.tb_M, wl.mgb,
+                  None if forced is None else forced[:, :n])
+        return time.perf_counter() - t0
+
+    n = min(wl.T, 64)
+    t = run(n)
+    if max_tokens is None:
+        max_tokens = wl.T
+    n2 = int(min(max_tokens, max(n, n * seconds / max(t, 1e-3))))
+    if n2 > n:
+        n = n2
+        t = run(n)
+    return {"value": wl.W * n / t, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens of each of the {wl.W} ranks "
+                      f"(route, plan, fp64 FFN, combine, scale), {t:.1f} s"}
+
+
+def reference_arm(args):
+    from tile_signaled_grouped_gb300.workloads import get_workload
+
+    wl = get_workload(args.workload)
+    per_step = max(5.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, seconds=1.0, max_tokens=16)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(wl, seconds=per_step))
+    wall = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "W": wl.W, "experts_per_rank": wl.L, "topk": wl.topk,
+                   "tokens_per_rank": wl.T, "d_model": wl.d_model, "d_ff": wl.d_ff,
+                   "tb_M": wl.tb_M, "mgb": wl.mgb},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "kind": "oracle",
+                         "cores": vals[0]["cores"], "sample": vals[-1]["sample"]},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--consumer-ctas", type=int, default=8)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * moe_tsg.h - C ABI of the tile-signalled grouped MoE expert-combine path (sm_103a).
+ *
+ * The path follows the TileMoE notes (zhongzhuzhou.org, "Fine-grained
+ * Computation-Communication Overlap via Tile-level Signaling and Scheduling
+ * for Mixture-of-Experts"):
+ *   routing (section 2.2 step 1) -> expert problem construction and combine
+ *   plan (section 4.2 row layout, 4.4 remote-first schedule / Algorithm 1,
+ *   4.5 combine plan) -> overlapped execution: a persistent grouped expert-FFN
+ *   producer that sets one ready flag per finished output tile, and a consumer
+ *   on a disjoint set of SMs that polls the flags and copies finished segments
+ *   (section 5.1-5.3) -> gated weighted sum (scale, section 2.2 step 5).
+ * The consumer signals each (sender, destination) group once, after one
+ * fence, as in the decoupled signalling of the Perseus summary
+ * (papercache.org, section 4.1, Algorithm 1).
+ *
+ * Everything runs on ONE GPU. The W expert-parallel ranks of the pages are
+ * logical: each has its own device allocations (token input, weights,
+ * rank workspace, receive buffer, output), and the combine all-to-all is a
+ * device-memory copy between those allocations.
+ *
+ * Conventions
+ *  - All pointers are device pointers unless stated. The caller owns all
+ *    memory; the library never allocates device memory and owns no stream.
+ *  - Tensors are dense, row-major, bf16 unless stated; base pointers must be
+ *    16-byte aligned. d_model and d_ff must be multiples of 128.
+ *  - Return value 0 (MOE_OK) or a negative MOE_ERR_* for errors detected on
+ *    the host before anything is enqueued. Errors detected on the device
+ *    (bad routing ids, a device wait that ran out of time) are sticky in the
+ *    plan workspace and are read with moe_status().
+ *  - Every call is asynchronous on the given stream(s) except moe_status(),
+ *    moe_timings() and the pure-host queries.
+ */
+#ifndef MOE_TSG_H
+#define MOE_TSG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+/* Largest number of logical ranks one plan can hold. */
+#define MOE_MAX_RANKS 8
+
+enum moe_error {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,         /* invalid configuration or argument */
+  MOE_ERR_WORKSPACE = -2,   /* a workspace is smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = -3,        /* a CUDA runtime call failed (no device, launch error) */
+  MOE_ERR_UNSUPPORTED = -4, /* the device is not sm_103 / the shape is outside the kernels' limits */
+  /* Device-side codes, reported through moe_status(). */
+  MOE_DEV_ROUTING = 1,      /* an expert id is out of range or repeated within a token */
+  MOE_DEV_TIMEOUT = 2       /* a device-side wait exceeded cfg.timeout_ns */
+};
+
+/* Configuration of one MoE layer split over W logical ranks.
+ * Expert e is owned by rank e / L (local index e % L), the placement of
+ * Figure 2b of the TileMoE notes. */
+typedef struct moe_cfg {
+  int W;             /* logical expert-parallel ranks, 1..MOE_MAX_RANKS */
+  int L;             /* experts per rank (E = W*L, 1..1024) */
+  int topk;          /* experts per token, 1..min(E, 32) */
+  int T;             /* tokens per rank, >= 1 */
+  int d_model;       /* D, multiple of 128 */
+  int d_ff;          /* F, expert hidden size, multiple of 128 */
+  int tb_M;          /* row-band height of the layout: 64, 128 or 256 */
+  int mgb;           /* row bands merged into one middle segment (section 5.2), >= 1 */
+  int consumer_ctas; /* consumer CTAs running beside the producer (cCTA of section 5.3).
+                        0 = serial: the producer uses every SM, then the consumer runs
+                        on every SM after it, on the producer stream. */
+  long long timeout_ns; /* bound on every device-side wait; <= 0 selects 2 s */
+} moe_cfg;
+
+/* Opaque host-side handle; holds the configuration, the carved workspace
+ * pointers and a few CUDA events. Created by moe_plan_create(). */
+typedef struct moe_plan moe_plan;
+
+/* Sizes of the caller-provided memory for cfg (pure host arithmetic).
+ *  plan_bytes:  one device allocation shared by all ranks (plan arrays, flags).
+ *  rank_bytes:  one device allocation per rank (its expert input X, hidden
+ *               activations and expert outputs Y, sized for the worst case).
+ *  recv_rows:   rows of the receive buffer every rank needs ([recv_rows, D] bf16);
+ *               the worst case T*topk.
+ * Any output pointer may be NULL. */
+int moe_workspace_size(const moe_cfg *cfg, size_t *plan_bytes, size_t *rank_bytes,
+                       int *recv_rows);
+
+/* Bind a configuration to its workspaces. plan_ws: plan_bytes; rank_ws: W pointers,
+ * each rank_bytes. Queries the current device; fails with MOE_ERR_UNSUPPORTED
+ * on anything other than compute capability 10.3. *out must be released with
+ * moe_plan_destroy(). Host memory only; enqueues nothing. */
+int moe_plan_create(const moe_cfg *cfg, void *plan_ws, size_t plan_ws_bytes,
+                    void *const *rank_ws, size_t rank_ws_bytes, moe_plan **out);
+void moe_plan_destroy(moe_plan *plan);
+
+/* Routing (TileMoE notes section 2.1 and 2.2 step 1): for every token, softmax over
+ * the E gate logits, then the topk experts with the largest logits in descending
+ * order (equal logits: the lower expert id first). The weights are the softmax
+ * probabilities at the chosen ids, not renormalised.
+ *  logits:     [W][T][E] fp32.
+ *  forced_ids: NULL, or [W][T][topk] int32 prescribed routing; then ids = forced_ids
+ *              and the weights are the probabilities at those ids.
+ *  topk_ids:   out [W][T][topk] int32.   topk_w: out [W][T][topk] fp32. */
+int moe_route(moe_plan *plan, const float *logits, const int32_t *forced_ids,
+              int32_t *topk_ids, float *topk_w, moe_stream_t stream);
+
+/* Expert problem construction and combine plan (TileMoE notes section 4.2, 4.4
+ * Algorithm 1, 4.5, 5.2) for all ranks, then the layout gather that fills each
+ * owner's expert input X with its tokens' rows (zero rows for padding).
+ *  topk_ids: [W][T][topk] int32, ids distinct within a token.
+ *  x:        W pointers, rank s's tokens [T][D] bf16.
+ * Ids out of range or repeated set MOE_DEV_ROUTING; the offending assignments are
+ * skipped. No device-to-host transfer: every size is read on the device. */
+int moe_plan_build(moe_plan *plan, const int32_t *topk_ids, const void *const *x,
+                   moe_stream_t stream);
+
+/* Overlapped expert FFN and combine (TileMoE notes section 5.1-5.3).
+ * The producer walks the remote-first schedule: per 128-row tile of X,
+ * h = SiLU(X Wg^T) * (X Wu^T) (bf16), then Y = h Wd^T (bf16), fp32 accumulation,
+ * and after each finished Y tile it sets that tile's ready flag. The consumer
+ * (consumer_ctas CTAs on a high-priority stream, or after the producer in serial
+ * mode) polls the flags and copies each finished segment's valid rows into the
+ * destination rank's receive buffer at the planned offset. Padding rows are never
+ * copied. Local rows stay in the owner's Y.
+ *  w_gate, w_up: W pointers, [L][F][D] bf16.  w_down: W pointers, [L][D][F] bf16.
+ *  recv:         W pointers, [recv_rows][D] bf16 (moe_workspace_size).
+ *  producer, consumer: streams; the consumer stream should have higher priority.
+ *  When consumer_ctas == 0 or both streams are equal, the call runs serially on
+ *  `producer`. On return, work enqueued later on `producer` is ordered after both
+ *  kernels. */
+int moe_expert_combine(moe_plan *plan, const void *const *w_gate, const void *const *w_up,
+                       const void *const *w_down, void *const *recv,
+                       moe_stream_t producer, moe_stream_t consumer);
+
+/* Scale (TileMoE notes section 2.2 step 5): out_s[t] = sum_j w[s][t][j] * y_j, where
+ * y_j is token (s,t)'s output of its j-th expert, read from rank s's receive buffer
+ * (remote expert) or rank s's own Y (local expert). fp32 accumulation in slot order,
+ * bf16 result.
+ *  topk_w: [W][T][topk] fp32.  recv: W pointers as given to moe_expert_combine.
+ *  out:    W pointers, [T][D] bf16. */
+int moe_scale(moe_plan *plan, const float *topk_w, const void *const *recv, void *const *out,
+              moe_stream_t stream);
+
+/* Synchronises `stream` and reads the device status word: *code is 0 or a
+ * MOE_DEV_* value, *detail the first failing item (token, band or tile index).
+ * The status stays set until moe_status_clear(). */
+int moe_status(moe_plan *plan, moe_stream_t stream, int *code, int *detail);
+int moe_status_clear(moe_plan *plan, moe_stream_t stream);
+
+/* Named arrays of the plan workspace and the rank workspaces, for inspection:
+ * byte offset of the array inside its workspace and its element count. Elements
+ * are int32 except MOE_RANK_X/H/Y (bf16). Pure host arithmetic. */
+enum moe_field {
+  MOE_PLAN_CNT = 0,          /* [E][W] rows of expert e from rank s */
+  MOE_PLAN_GROUP_START,      /* [E][W] first row of group (e, s) in expert e's block */
+  MOE_PLAN_RECV_OFF,         /* [E][W] first receive row of (e, s) at rank s, -1 if local */
+  MOE_PLAN_EXPERT_START,     /* [E]    first row of expert e's block in its owner's X */
+  MOE_PLAN_ROWS_ALLOC,       /* [E]    rows of expert e's block (multiple of tb_M) */
+  MOE_PLAN_NRB,              /* [E]    remote row bands of expert e */
+  MOE_PLAN_RANK_ROWS,        /* [W]    rows of each owner's X */
+  MOE_PLAN_RANK_NREMOTE,     /* [W]    remote prefix length of each owner's schedule */
+  MOE_PLAN_RECV_ROWS,        /* [W]    rows received by each rank */
+  MOE_PLAN_RANK_NSEG,        /* [W]    segments of each owner */
+  MOE_PLAN_BAND_EXPERT,      /* [W][NBmax] per rank-local band: expert */
+  MOE_PLAN_BAND_DST,         /* [W][NBmax] destination rank */
+  MOE_PLAN_BAND_VALID,       /* [W][NBmax] valid (non-padding) rows */
+  MOE_PLAN_BAND_DST_ROW,     /* [W][NBmax] first receive row at the destination, -1 if local */
+  MOE_PLAN_SCHEDULE,         /* [W][NBmax] S: rank-local band ids in schedule order */
+  MOE_PLAN_SEG_FIRST,        /* [W][NBmax] first schedule index of each segment */
+  MOE_PLAN_SEG_NBANDS,       /* [W][NBmax] bands of each segment */
+  MOE_PLAN_XSRC,             /* [W][RowsMax] per X row: source token s*T+t, or -1 */
+  MOE_PLAN_SCALE_SRC,        /* [W][T][topk] >= 0: receive row; < 0: row -v-1 of own Y */
+  MOE_PLAN_TOTALS,           /* [8] 0: tiles, 1: segments, 2: tile units, 3: bands */
+  MOE_PLAN_TILE_ROW,         /* [tiles] per 128-row producer tile: rank*2^24 + first X row */
+  MOE_PLAN_TILE_EXPERT,      /* [tiles] expert of each producer tile */
+  MOE_PLAN_SEG_ORDER,        /* [segments] consumer order: rank*NBmax + segment */
+  MOE_PLAN_STATUS,           /* [4] device status word */
+  MOE_PLAN_FLAGS,            /* [W][NBmax][D/tile_N] ready flags of the last combine */
+  MOE_PLAN_GROUP_SIG,        /* [W][W] group signals (sender, destination) of the last combine */
+  MOE_PLAN_NFIELDS,
+  MOE_RANK_X = 100,          /* [RowsMax][D] bf16 expert input */
+  MOE_RANK_H,                /* [RowsMax][F] bf16 hidden activation */
+  MOE_RANK_Y                 /* [RowsMax][D] bf16 expert output */
+};
+int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count);
+
+/* Elapsed device time in ms of the kernels enqueued by the last calls, measured
+ * with CUDA events recorded on the stream each kernel ran on. Synchronises on the
+ * events. Order: [0] route, [1] plan (all plan kernels and the gather),
+ * [2] producer, [3] consumer, [4] scale, [5] gather only. A slot with no
+ * measurement is -1. Pure instrumentation; records events only when enabled. */
+int moe_set_timing(moe_plan *plan, int enable);
+int moe_timings(moe_plan *plan, float *ms, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_TSG_H */

@@ -1,0 +1,149 @@
+"""Parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Plan arrays (layout, schedule, combine plan, segments, scale map) and the
+layout gather and combine copies are compared bit-exactly; FFN rows and the
+final outputs within max-abs 2e-2 and relative L2 5e-3 of the float64 oracle.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+from tests import parity as P  # noqa: E402
+from tile_signaled_grouped_gb300 import capi  # noqa: E402
+from tile_signaled_grouped_gb300.workloads import Workload, get_workload  # noqa: E402
+
+
+def _full_check(wl, mode="overlap", cctas=8):
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode=mode, consumer_ctas=cctas)
+    assert layer.status() == (0, 0)
+    ids, w, plan = P.oracle_plan(wl, inp)
+    P.check_plan(layer, wl, plan, ids, w)
+    P.check_order(layer, wl, plan)
+    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w)
+    layer.close()
+
+
+@pytest.mark.parametrize("mode", ["serial", "overlap"])
+@pytest.mark.parametrize("mgb", [1, 2])
+def test_tiny_full_parity(mode, mgb):
+    _full_check(get_workload("tiny", mgb=mgb), mode)
+
+
+SMALL = [
+    # ragged T, every band height, several ranks/experts; d_model 128 uses 128-wide GEMM2 tiles
+    Workload("ragged_tb64", W=3, L=3, topk=2, T=77, d_model=256, d_ff=384, tb_M=64, routing="gate", mgb=3),
+    Workload("ragged_tb128", W=4, L=2, topk=3, T=130, d_model=128, d_ff=256, tb_M=128, routing="gate"),
+    Workload("ragged_tb256", W=2, L=4, topk=2, T=301, d_model=384, d_ff=128, tb_M=256, routing="gate", mgb=2),
+    Workload("k_equals_E", W=2, L=2, topk=4, T=40, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("one_rank", W=1, L=3, topk=2, T=50, d_model=128, d_ff=256, tb_M=128, routing="gate"),
+    Workload("T1", W=4, L=2, topk=2, T=1, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("skew_small", W=4, L=4, topk=1, T=300, d_model=256, d_ff=256, tb_M=256, routing="zipf"),
+    Workload("balanced_small", W=4, L=2, topk=2, T=256, d_model=256, d_ff=512, tb_M=128, routing="balanced"),
+    Workload("eight_ranks", W=8, L=4, topk=4, T=64, d_model=256, d_ff=256, tb_M=64, routing="gate", mgb=2),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_small_shapes_full_parity(wl):
+    _full_check(wl, "overlap", cctas=4)
+
+
+def test_all_local_routing_sends_nothing():
+    wl = Workload("all_local", W=4, L=2, topk=2, T=96, d_model=128, d_ff=256, tb_M=64, routing="balanced")
+    inp = P.inputs_for(wl)
+    # every token of rank s routes to rank s's two experts
+    ids = torch.stack([torch.full((wl.T,), 2 * s, dtype=torch.int32) for s in range(4)])
+    inp.forced_ids = torch.stack([ids, ids + 1], dim=-1).cuda()
+    layer = P.run_gpu(wl, inp)
+    assert layer.status() == (0, 0)
+    ids_o, w, plan = P.oracle_plan(wl, inp)
+    assert plan.recv_rows.sum() == 0
+    P.check_plan(layer, wl, plan, ids_o, w)
+    P.check_layout_and_outputs(layer, wl, inp, plan, ids_o, w)
+
+
+FULL = ["a100_like", "qwen3_235b_like", "deepseek_v3_like", "stress_skew"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """The five workload shapes at full size, in the launch configuration the bench
+    times (producer and consumer overlapped on two streams): every plan array
+    bit-exact, sampled rows and tokens against the oracle, all copies exact."""
+    wl = get_workload(name)
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="overlap", consumer_ctas=16)
+    assert layer.status() == (0, 0)
+    ids, w, plan = P.oracle_plan(wl, inp)
+    P.check_plan(layer, wl, plan, ids, w)
+    P.check_order(layer, wl, plan)
+    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=12,
+                               rng=np.random.default_rng(1))
+
+
+def test_repeat_runs_are_identical():
+    wl = get_workload("tiny")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp)
+    first = [layer.field(f).clone() for f in (capi.MOE_PLAN_SCHEDULE, capi.MOE_PLAN_XSRC,
+                                              capi.MOE_PLAN_SEG_FIRST, capi.MOE_PLAN_SCALE_SRC)]
+    out0 = [t.clone() for t in layer.out]
+    for _ in range(5):
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids)
+        torch.cuda.synchronize()
+        again = [layer.field(f) for f in (capi.MOE_PLAN_SCHEDULE, capi.MOE_PLAN_XSRC,
+                                          capi.MOE_PLAN_SEG_FIRST, capi.MOE_PLAN_SCALE_SRC)]
+        assert all(torch.equal(a, b) for a, b in zip(first, again))
+        assert all(torch.equal(a, b) for a, b in zip(out0, layer.out))
+    assert layer.status() == (0, 0)
+
+
+def test_bad_routing_is_reported_and_recoverable():
+    wl = get_workload("tiny")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp)
+    bad = layer.ids.clone()
+    bad[1, 3, 0] = wl.E + 5  # out of range
+    layer.plan_build(inp.x, ids=bad)
+    layer.expert_combine(inp.w_gate, inp.w_up, inp.w_down)
+    code, detail = layer.status()
+    assert code == capi.MOE_DEV_ROUTING and detail == 1 * wl.T + 3
+    layer.clear_status()
+    layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids)
+    assert layer.status() == (0, 0)
+
+
+def test_device_wait_timeout_is_reported_and_recoverable():
+    """A wait bound far shorter than the producer's work makes the consumer's flag
+    wait run out: the kernels return, the status says MOE_DEV_TIMEOUT, and the
+    context stays usable for a normal run afterwards."""
+    wl = get_workload("a100_like")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, timeout_ns=20_000)  # 20 us
+    code, _ = layer.status()
+    assert code == capi.MOE_DEV_TIMEOUT
+    layer.close()
+    layer = P.run_gpu(wl, inp)
+    assert layer.status() == (0, 0)
+
+
+def test_host_argument_errors():
+    wl = get_workload("tiny")
+    cfg = capi.moe_cfg(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, 1, 4, 0)
+    pb, rb, _ = capi.moe_workspace_size(cfg)
+    plan_ws = torch.zeros(pb, dtype=torch.uint8, device="cuda")
+    rank = [torch.zeros(rb + 1024, dtype=torch.uint8, device="cuda") for _ in range(wl.W)]
+    ptrs = [t.data_ptr() + (-t.data_ptr()) % 1024 for t in rank]
+    with pytest.raises(capi.MoeError, match="WORKSPACE"):
+        capi.moe_plan_create(cfg, plan_ws.data_ptr(), pb - 256, ptrs, rb)
+    with pytest.raises(capi.MoeError, match="ARG"):
+        capi.moe_plan_create(cfg, plan_ws.data_ptr() + 4, pb, ptrs, rb)
+    plan = capi.moe_plan_create(cfg, plan_ws.data_ptr(), pb, ptrs, rb)
+    with pytest.raises(capi.MoeError, match="ARG"):
+        capi.moe_plan_build(plan, 0, [0] * wl.W, 0)
+    capi.moe_plan_destroy(plan)

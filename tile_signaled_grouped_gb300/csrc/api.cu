@@ -1,0 +1,439 @@
+// Host side of the C ABI: configuration checks, workspace carving, tensor maps
+// and the stream choreography of the overlapped producer and consumer.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "moe_common.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+enum TimingSlot { kTRoute = 0, kTPlan, kTProducer, kTConsumer, kTScale, kTGather, kTSlots };
+
+}  // namespace
+
+struct moe_plan {
+  moe_cfg cfg;
+  Dims d;
+  uint8_t* plan_ws;
+  uint8_t* rank_ws[MOE_MAX_RANKS];
+  size_t offsets[PA_COUNT];
+  size_t counts[PA_COUNT];
+  RankLayout rl;
+  int num_sms;
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  cudaEvent_t ev_ready, ev_join;
+  cudaEvent_t ev_t0[kTSlots], ev_t1[kTSlots];
+  bool recorded[kTSlots];
+  bool timing;
+};
+
+namespace moe {
+
+int dims_from_cfg(const moe_cfg* c, Dims* d) {
+  if (c == nullptr || d == nullptr) return MOE_ERR_ARG;
+  if (c->W < 1 || c->W > MOE_MAX_RANKS || c->L < 1 || c->L > 256) return MOE_ERR_ARG;
+  const long long E = (long long)c->W * c->L;
+  if (E > 1024 || c->topk < 1 || c->topk > std::min<long long>(E, 32)) return MOE_ERR_ARG;
+  if (c->T < 1 || c->T > (1 << 20)) return MOE_ERR_ARG;
+  if (c->d_model < 128 || c->d_model % 128 || c->d_ff < 128 || c->d_ff % 128) return MOE_ERR_ARG;
+  if (c->d_model > 65536 || c->d_ff > 65536) return MOE_ERR_ARG;
+  if (c->tb_M != 64 && c->tb_M != 128 && c->tb_M != 256) return MOE_ERR_ARG;
+  if (c->mgb < 1 || c->consumer_ctas < 0) return MOE_ERR_ARG;
+  Dims x{};
+  x.W = c->W;
+  x.L = c->L;
+  x.E = (int)E;
+  x.k = c->topk;
+  x.T = c->T;
+  x.D = c->d_model;
+  x.F = c->d_ff;
+  x.tb = c->tb_M;
+  x.mgb = c->mgb;
+  x.TW = (c->T + 31) / 32;
+  // Worst case rows of one owner: every token reaching min(k, L) of its experts,
+  // plus at most tb-1 zero rows per (expert, source rank) group.
+  const long long rm = (long long)c->W * c->T * std::min(c->topk, c->L) +
+                       (long long)c->L * c->W * (c->tb_M - 1);
+  const long long RM = (rm + c->tb_M - 1) / c->tb_M * c->tb_M;
+  if (RM >= (1LL << 24)) return MOE_ERR_UNSUPPORTED;
+  x.RM = (int)RM;
+  x.NBM = x.RM / x.tb;
+  x.parts = x.tb >= kTileM ? x.tb / kTileM : 1;
+  x.NMM = x.NBM * x.parts;
+  x.N2 = x.D % 256 == 0 ? 256 : 128;
+  x.nt1 = x.F / kN1;
+  x.nt2 = x.D / x.N2;
+  *d = x;
+  return MOE_OK;
+}
+
+size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
+  size_t n[PA_COUNT] = {};
+  const size_t W = d.W, E = d.E, NBM = d.NBM, NMM = d.NMM;
+  n[PA_STATUS] = 4;
+  n[PA_TOTALS] = 8;
+  n[PA_QUEUE] = 4;
+  n[PA_G1CNT] = W * NMM;
+  n[PA_FLAGS] = W * NBM * d.nt2;
+  n[PA_GROUP_DONE] = W * W;
+  n[PA_GROUP_SIG] = W * W;
+  n[PA_BITMAP] = E * W * d.TW;
+  n[PA_WPRE] = E * W * d.TW;
+  n[PA_CNT] = n[PA_GROUP_START] = n[PA_RECV_OFF] = E * W;
+  n[PA_EXPERT_START] = n[PA_ROWS_ALLOC] = n[PA_NB] = n[PA_NRB] = E;
+  n[PA_RANK_ROWS] = n[PA_RANK_NB] = n[PA_RANK_NREMOTE] = n[PA_RECV_ROWS] = n[PA_RANK_NSEG] = W;
+  n[PA_RANK_NMT] = n[PA_RANK_NMT_REMOTE] = W;
+  n[PA_BAND_EXPERT] = n[PA_BAND_DST] = n[PA_BAND_VALID] = n[PA_BAND_DST_ROW] = W * NBM;
+  n[PA_BAND_TILE] = W * NBM;
+  n[PA_SCHED] = n[PA_SEG_FIRST] = n[PA_SEG_NB] = n[PA_SEG_GIDX] = W * NBM;
+  n[PA_GROUP_NSEG] = W * W;
+  n[PA_RANK_TILES] = 2 * W * NMM;
+  n[PA_TILE_ROW] = n[PA_TILE_EXPERT] = W * NMM;
+  n[PA_UNIT_BEGIN] = W * (NMM / kTileGroup + 2) + 1;
+  n[PA_SEG_ORDER] = W * NBM;
+  n[PA_XSRC] = W * (size_t)d.RM;
+  n[PA_SCALE_SRC] = W * (size_t)d.T * d.k;
+  size_t pos = 0;
+  for (int i = 0; i < PA_COUNT; ++i) {
+    if (off) off[i] = pos;
+    if (cnt) cnt[i] = n[i];
+    // The per-combine zeroed arrays are packed back to back (one memset).
+    const bool packed = i >= PA_QUEUE && i < PA_GROUP_SIG;
+    pos += packed ? n[i] * 4 : align_up(n[i] * 4, kAlign);
+  }
+  return align_up(pos, kAlign);
+}
+
+RankLayout rank_layout(const Dims& d) {
+  RankLayout r{};
+  const size_t xb = align_up((size_t)d.RM * d.D * 2, 1024);
+  const size_t hb = align_up((size_t)d.RM * d.F * 2, 1024);
+  r.x_off = 0;
+  r.h_off = xb;
+  r.y_off = xb + hb;
+  r.bytes = xb + hb + xb;
+  return r;
+}
+
+}  // namespace moe
+
+namespace {
+
+#define CUDA_TRY(x)                      \
+  do {                                   \
+    if ((x) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+DevPlan dev_plan(const moe_plan* p) {
+  DevPlan dp{};
+  dp.d = p->d;
+  for (int i = 0; i < PA_COUNT; ++i)
+    dp.a[i] = reinterpret_cast<int32_t*>(p->plan_ws + p->offsets[i]);
+  dp.timeout_ns = p->cfg.timeout_ns > 0 ? p->cfg.timeout_ns : 2000000000LL;
+  return dp;
+}
+
+bool aligned16(const void* ptr) { return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+void tstart(moe_plan* p, int slot, cudaStream_t s) {
+  if (p->timing) cudaEventRecord(p->ev_t0[slot], s);
+}
+void tstop(moe_plan* p, int slot, cudaStream_t s) {
+  if (p->timing) {
+    cudaEventRecord(p->ev_t1[slot], s);
+    p->recorded[slot] = true;
+  }
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box = box_rows x 64
+// columns (128 B, the swizzle span), 128-byte swizzle, zero fill out of bounds.
+bool make_map(const moe_plan* p, CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBlockK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = p->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_workspace_size(const moe_cfg* cfg, size_t* plan_bytes, size_t* rank_bytes, int* recv_rows) {
+  Dims d;
+  const int rc = dims_from_cfg(cfg, &d);
+  if (rc != MOE_OK) return rc;
+  if (plan_bytes) *plan_bytes = plan_layout(d, nullptr, nullptr);
+  if (rank_bytes) *rank_bytes = rank_layout(d).bytes;
+  if (recv_rows) *recv_rows = d.T * d.k;
+  return MOE_OK;
+}
+
+int moe_field(const moe_cfg* cfg, int field, size_t* byte_offset, size_t* count) {
+  Dims d;
+  const int rc = dims_from_cfg(cfg, &d);
+  if (rc != MOE_OK) return rc;
+  if (field >= MOE_RANK_X && field <= MOE_RANK_Y) {
+    const RankLayout r = rank_layout(d);
+    const size_t offs[3] = {r.x_off, r.h_off, r.y_off};
+    const size_t cols[3] = {(size_t)d.D, (size_t)d.F, (size_t)d.D};
+    if (byte_offset) *byte_offset = offs[field - MOE_RANK_X];
+    if (count) *count = (size_t)d.RM * cols[field - MOE_RANK_X];
+    return MOE_OK;
+  }
+  static const int map[MOE_PLAN_NFIELDS] = {
+      PA_CNT,          PA_GROUP_START, PA_RECV_OFF,   PA_EXPERT_START, PA_ROWS_ALLOC,
+      PA_NRB,          PA_RANK_ROWS,   PA_RANK_NREMOTE, PA_RECV_ROWS,  PA_RANK_NSEG,
+      PA_BAND_EXPERT,  PA_BAND_DST,    PA_BAND_VALID, PA_BAND_DST_ROW, PA_SCHED,
+      PA_SEG_FIRST,    PA_SEG_NB,      PA_XSRC,       PA_SCALE_SRC,    PA_TOTALS,
+      PA_TILE_ROW,     PA_TILE_EXPERT, PA_SEG_ORDER,  PA_STATUS,       PA_FLAGS,
+      PA_GROUP_SIG};
+  if (field < 0 || field >= MOE_PLAN_NFIELDS) return MOE_ERR_ARG;
+  size_t off[PA_COUNT], cnt[PA_COUNT];
+  plan_layout(d, off, cnt);
+  if (byte_offset) *byte_offset = off[map[field]];
+  if (count) *count = cnt[map[field]];
+  return MOE_OK;
+}
+
+int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, void* const* rank_ws,
+                    size_t rank_ws_bytes, moe_plan** out) {
+  if (out == nullptr) return MOE_ERR_ARG;
+  *out = nullptr;
+  Dims d;
+  int rc = dims_from_cfg(cfg, &d);
+  if (rc != MOE_OK) return rc;
+  if (!aligned16(plan_ws) || rank_ws == nullptr) return MOE_ERR_ARG;
+  for (int r = 0; r < d.W; ++r)
+    if (!aligned16(rank_ws[r]) || (reinterpret_cast<uintptr_t>(rank_ws[r]) & 1023)) return MOE_ERR_ARG;
+  size_t off[PA_COUNT], cnt[PA_COUNT];
+  const size_t need = plan_layout(d, off, cnt);
+  const RankLayout rl = rank_layout(d);
+  if (plan_ws_bytes < need || rank_ws_bytes < rl.bytes) return MOE_ERR_WORKSPACE;
+
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;
+
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      fn == nullptr || q != cudaDriverEntryPointSuccess)
+    return MOE_ERR_CUDA;
+
+  moe_plan* p = new (std::nothrow) moe_plan();
+  if (p == nullptr) return MOE_ERR_ARG;
+  p->cfg = *cfg;
+  p->d = d;
+  p->plan_ws = static_cast<uint8_t*>(plan_ws);
+  for (int r = 0; r < d.W; ++r) p->rank_ws[r] = static_cast<uint8_t*>(rank_ws[r]);
+  std::memcpy(p->offsets, off, sizeof(off));
+  std::memcpy(p->counts, cnt, sizeof(cnt));
+  p->rl = rl;
+  p->num_sms = prop.multiProcessorCount;
+  p->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  bool ok = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; i < kTSlots && ok; ++i)
+    ok = cudaEventCreate(&p->ev_t0[i]) == cudaSuccess && cudaEventCreate(&p->ev_t1[i]) == cudaSuccess;
+  if (!ok) {
+    moe_plan_destroy(p);
+    return MOE_ERR_CUDA;
+  }
+  if (p->cfg.consumer_ctas >= p->num_sms) p->cfg.consumer_ctas = p->num_sms / 2;
+  *out = p;
+  return MOE_OK;
+}
+
+void moe_plan_destroy(moe_plan* p) {
+  if (p == nullptr) return;
+  if (p->ev_ready) cudaEventDestroy(p->ev_ready);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  for (int i = 0; i < kTSlots; ++i) {
+    if (p->ev_t0[i]) cudaEventDestroy(p->ev_t0[i]);
+    if (p->ev_t1[i]) cudaEventDestroy(p->ev_t1[i]);
+  }
+  delete p;
+}
+
+int moe_route(moe_plan* p, const float* logits, const int32_t* forced, int32_t* ids, float* w,
+              moe_stream_t stream) {
+  if (p == nullptr || !aligned16(logits) || ids == nullptr || w == nullptr) return MOE_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const DevPlan dp = dev_plan(p);
+  tstart(p, kTRoute, s);
+  CUDA_TRY(launch_route(dp, logits, forced, ids, w, s));
+  tstop(p, kTRoute, s);
+  return MOE_OK;
+}
+
+int moe_plan_build(moe_plan* p, const int32_t* ids, const void* const* x, moe_stream_t stream) {
+  if (p == nullptr || ids == nullptr || x == nullptr) return MOE_ERR_ARG;
+  for (int r = 0; r < p->d.W; ++r)
+    if (!aligned16(x[r])) return MOE_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const DevPlan dp = dev_plan(p);
+  tstart(p, kTPlan, s);
+  CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_BITMAP], 0, p->counts[PA_BITMAP] * 4, s));
+  CUDA_TRY(launch_plan(dp, ids, s));
+  const __nv_bfloat16* xs[MOE_MAX_RANKS] = {};
+  __nv_bfloat16* xb[MOE_MAX_RANKS] = {};
+  for (int r = 0; r < p->d.W; ++r) {
+    xs[r] = static_cast<const __nv_bfloat16*>(x[r]);
+    xb[r] = reinterpret_cast<__nv_bfloat16*>(p->rank_ws[r] + p->rl.x_off);
+  }
+  tstart(p, kTGather, s);
+  CUDA_TRY(launch_gather(dp, xs, xb, p->num_sms, s));
+  tstop(p, kTGather, s);
+  tstop(p, kTPlan, s);
+  return MOE_OK;
+}
+
+int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const* w_up,
+                       const void* const* w_down, void* const* recv, moe_stream_t producer,
+                       moe_stream_t consumer) {
+  if (p == nullptr || w_gate == nullptr || w_up == nullptr || w_down == nullptr || recv == nullptr)
+    return MOE_ERR_ARG;
+  const Dims& d = p->d;
+  for (int r = 0; r < d.W; ++r)
+    if (!aligned16(w_gate[r]) || !aligned16(w_up[r]) || !aligned16(w_down[r]) || !aligned16(recv[r]))
+      return MOE_ERR_ARG;
+  cudaStream_t sp = reinterpret_cast<cudaStream_t>(producer);
+  cudaStream_t sc = reinterpret_cast<cudaStream_t>(consumer);
+  const bool serial = p->cfg.consumer_ctas == 0 || sp == sc;
+  const int cgrid = serial ? p->num_sms : p->cfg.consumer_ctas;
+  const int pgrid = serial ? p->num_sms : p->num_sms - p->cfg.consumer_ctas;
+
+  ProducerArgs pa;
+  std::memset(&pa, 0, sizeof(pa));
+  pa.p = dev_plan(p);
+  for (int r = 0; r < d.W; ++r) {
+    uint8_t* ws = p->rank_ws[r];
+    const void* X = ws + p->rl.x_off;
+    __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(ws + p->rl.h_off);
+    __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(ws + p->rl.y_off);
+    if (!make_map(p, &pa.tm_x[r], X, d.RM, d.D, kTileM) ||
+        !make_map(p, &pa.tm_h[r], H, d.RM, d.F, kTileM) ||
+        !make_map(p, &pa.tm_wg[r], w_gate[r], (uint64_t)d.L * d.F, d.D, kN1) ||
+        !make_map(p, &pa.tm_wu[r], w_up[r], (uint64_t)d.L * d.F, d.D, kN1) ||
+        !make_map(p, &pa.tm_wd[r], w_down[r], (uint64_t)d.L * d.D, d.F, d.N2))
+      return MOE_ERR_ARG;
+    pa.h[r] = H;
+    pa.y[r] = Y;
+  }
+  const int per_unit = kTileGroup * (d.nt1 + d.nt2);
+  pa.lag = (2 * pgrid + per_unit - 1) / per_unit + 1;
+
+  ConsumerArgs ca;
+  std::memset(&ca, 0, sizeof(ca));
+  ca.p = pa.p;
+  for (int r = 0; r < d.W; ++r) {
+    ca.y[r] = pa.y[r];
+    ca.recv[r] = static_cast<__nv_bfloat16*>(recv[r]);
+  }
+  const int groups = std::max(1, d.W * (d.W - 1));
+  ca.parts_per_group = std::max(1, (cgrid + groups - 1) / groups);
+
+  // Ready flags, GEMM1 counters, the ticket counter and the group signals start at 0.
+  const size_t z0 = p->offsets[PA_QUEUE];
+  const size_t z1 = p->offsets[PA_GROUP_SIG] + p->counts[PA_GROUP_SIG] * 4;
+  CUDA_TRY(cudaMemsetAsync(p->plan_ws + z0, 0, z1 - z0, sp));
+  if (serial) {
+    tstart(p, kTProducer, sp);
+    CUDA_TRY(launch_producer(pa, pgrid, sp));
+    tstop(p, kTProducer, sp);
+    tstart(p, kTConsumer, sp);
+    CUDA_TRY(launch_consumer(ca, cgrid, sp));
+    tstop(p, kTConsumer, sp);
+  } else {
+    CUDA_TRY(cudaEventRecord(p->ev_ready, sp));
+    CUDA_TRY(cudaStreamWaitEvent(sc, p->ev_ready, 0));
+    tstart(p, kTConsumer, sc);
+    CUDA_TRY(launch_consumer(ca, cgrid, sc));
+    tstop(p, kTConsumer, sc);
+    CUDA_TRY(cudaEventRecord(p->ev_join, sc));
+    tstart(p, kTProducer, sp);
+    CUDA_TRY(launch_producer(pa, pgrid, sp));
+    tstop(p, kTProducer, sp);
+    CUDA_TRY(cudaStreamWaitEvent(sp, p->ev_join, 0));
+  }
+  return MOE_OK;
+}
+
+int moe_scale(moe_plan* p, const float* topk_w, const void* const* recv, void* const* out,
+              moe_stream_t stream) {
+  if (p == nullptr || topk_w == nullptr || recv == nullptr || out == nullptr) return MOE_ERR_ARG;
+  const Dims& d = p->d;
+  ScaleArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = dev_plan(p);
+  a.w = topk_w;
+  for (int r = 0; r < d.W; ++r) {
+    if (!aligned16(recv[r]) || !aligned16(out[r])) return MOE_ERR_ARG;
+    a.recv[r] = static_cast<const __nv_bfloat16*>(recv[r]);
+    a.y[r] = reinterpret_cast<const __nv_bfloat16*>(p->rank_ws[r] + p->rl.y_off);
+    a.out[r] = static_cast<__nv_bfloat16*>(out[r]);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  tstart(p, kTScale, s);
+  CUDA_TRY(launch_scale(a, p->num_sms, s));
+  tstop(p, kTScale, s);
+  return MOE_OK;
+}
+
+int moe_status(moe_plan* p, moe_stream_t stream, int* code, int* detail) {
+  if (p == nullptr) return MOE_ERR_ARG;
+  CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  uint32_t st[2] = {0, 0};
+  CUDA_TRY(cudaMemcpy(st, p->plan_ws + p->offsets[PA_STATUS], sizeof(st), cudaMemcpyDeviceToHost));
+  if (code) *code = (int)st[0];
+  if (detail) *detail = (int)st[1];
+  return MOE_OK;
+}
+
+int moe_status_clear(moe_plan* p, moe_stream_t stream) {
+  if (p == nullptr) return MOE_ERR_ARG;
+  CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_STATUS], 0, 16,
+                           reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_set_timing(moe_plan* p, int enable) {
+  if (p == nullptr) return MOE_ERR_ARG;
+  p->timing = enable != 0;
+  for (int i = 0; i < kTSlots; ++i) p->recorded[i] = false;
+  return MOE_OK;
+}
+
+int moe_timings(moe_plan* p, float* ms, int n) {
+  if (p == nullptr || ms == nullptr) return MOE_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    ms[i] = -1.f;
+    if (i >= kTSlots || !p->recorded[i]) continue;
+    CUDA_TRY(cudaEventSynchronize(p->ev_t1[i]));
+    float v = 0.f;
+    CUDA_TRY(cudaEventElapsedTime(&v, p->ev_t0[i], p->ev_t1[i]));
+    ms[i] = v;
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// Gate routing and the gated weighted sum (scale).
+//
+// TileMoE notes (zhongzhuzhou.org), section 2.1 and 2.2 steps 1 and 5: the
+// router forms a probability distribution over the E experts per token and
+// keeps the top k; the owner rank combines the k expert outputs of a token
+// with the gate weights.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxPerLane = 32;  // E <= 1024
+
+// One warp per token: softmax over E logits (fp32), then k rounds of a warp
+// argmax on (logit descending, expert id ascending). Comparing logits decides
+// the same order as comparing probabilities, without rounding ties.
+__global__ void route_kernel(DevPlan p, const float* __restrict__ logits,
+                             const int32_t* __restrict__ forced, int32_t* __restrict__ ids,
+                             float* __restrict__ w) {
+  const Dims d = p.d;
+  const int lane = threadIdx.x & 31;
+  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (tok >= d.W * d.T) return;
+  const float* lg = logits + (size_t)tok * d.E;
+  float v[kMaxPerLane];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < d.E ? lg[e] : -INFINITY;
+    mx = fmaxf(mx, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i)
+    if (lane + 32 * i < d.E) sum += expf(v[i] - mx);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = 1.0f / sum;
+
+  if (forced != nullptr) {
+    for (int j = lane; j < d.k; j += 32) {
+      const int e = forced[(size_t)tok * d.k + j];
+      ids[(size_t)tok * d.k + j] = e;
+      w[(size_t)tok * d.k + j] = (e >= 0 && e < d.E) ? expf(lg[e] - mx) * inv : 0.f;
+    }
+    return;
+  }
+  uint32_t taken = 0;  // bit i: this lane's candidate i already chosen
+  for (int j = 0; j < d.k; ++j) {
+    float bv = -INFINITY;
+    int be = INT_MAX, bi = -1;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < d.E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+        bi = i;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (bi >= 0 && lane + 32 * bi == be) taken |= 1u << bi;
+    if (lane == 0) {
+      ids[(size_t)tok * d.k + j] = be;
+      w[(size_t)tok * d.k + j] = expf(bv - mx) * inv;
+    }
+  }
+}
+
+// One warp per token (s, t): out_s[t] = sum_j w_j * row_j, fp32 in slot order.
+__global__ void scale_kernel(const __grid_constant__ ScaleArgs a) {
+  const Dims d = a.p.d;
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int n16 = d.D / 8;
+  for (int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < d.W * d.T; tok += warps) {
+    const int s = tok / d.T, t = tok % d.T;
+    const int32_t* src = a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k;
+    const float* wt = a.w + (size_t)tok * d.k;
+    uint4* out = reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D);
+    for (int c = lane; c < n16; c += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < d.k; ++j) {
+        const int sj = src[j];
+        if (sj == INT_MIN) continue;  // invalid routing slot (reported by the plan)
+        const __nv_bfloat16* row =
+            sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
+        const float wj = wt[j];
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(h[q]);
+          acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
+          acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
+        }
+      }
+      out[c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                          pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* forced,
+                         int32_t* ids, float* w, cudaStream_t s) {
+  const int ntok = p.d.W * p.d.T;
+  route_kernel<<<(ntok * 32 + 255) / 256, 256, 0, s>>>(p, logits, forced, ids, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s) {
+  scale_kernel<<<num_sms * 8, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
