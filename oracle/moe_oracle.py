@@ -47,6 +47,11 @@ design notes of the repository):
       SiLU(z) = z / (1 + exp(-z)). Padding rows are defined to produce 0.
   R10 The padding bound (W-1)(tb_M-1) of [TileMoE] 4.3/6 holds per (rank, local
       expert). The worked example of 11.10 applies it to one expert's tokens.
+  R11 Both expert GEMMs take half-precision operands ([TileMoE] 7.1: CUTLASS
+      GEMMs; 7.6: outputs agree with the serial baseline up to FP16 rounding).
+      Here the operands are bf16, so the hidden activation h = SiLU(g) * u, being
+      the second GEMM's input, is rounded to bf16 (to nearest, ties to even)
+      before W_down is applied. Everything else is float64.
 """
 from __future__ import annotations
 
@@ -55,7 +60,7 @@ import dataclasses
 import numpy as np
 
 __all__ = [
-    "softmax", "silu", "route", "Plan", "build_plan", "expert_ffn", "layout_rows",
+    "softmax", "silu", "round_bf16", "route", "Plan", "build_plan", "expert_ffn", "layout_rows",
     "rank_outputs", "buffer_row_outputs", "combine", "scale", "forward", "padding_bound",
 ]
 
@@ -332,15 +337,33 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
-def expert_ffn(xrows, w_gate, w_up, w_down) -> np.ndarray:
-    """y = W_down (SiLU(W_gate x) * (W_up x)) for each row x, in float64.
+def round_bf16(v) -> np.ndarray:
+    """Round to the nearest bfloat16 value, ties to even (returned as float64).
+
+    bf16 keeps the top 16 bits of an IEEE float32: round the float64 value to
+    float32 first (exact for every bf16 value), then round the low 16 bits of the
+    float32 pattern to nearest with ties to even. Inf and NaN are not expected.
+    """
+    f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> 16) & 1
+    bits = (bits + 0x7FFF + lsb) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def expert_ffn(xrows, w_gate, w_up, w_down, round_hidden: bool = True) -> np.ndarray:
+    """y = W_down h, h = SiLU(W_gate x) * (W_up x), for each row x.
 
     xrows [n, D]; w_gate, w_up [F, D]; w_down [D, F] (nn.Linear layout).
+    float64 throughout; h is rounded to bf16 before the second GEMM (reading R11)
+    unless round_hidden is False.
     """
     x = np.asarray(xrows, dtype=np.float64)
     g = x @ np.asarray(w_gate, dtype=np.float64).T
     u = x @ np.asarray(w_up, dtype=np.float64).T
     a = silu(g) * u
+    if round_hidden:
+        a = round_bf16(a)
     return a @ np.asarray(w_down, dtype=np.float64).T
 
 

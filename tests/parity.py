@@ -1,8 +1,13 @@
 """Helpers shared by the GPU parity tests: run the CUDA path, build the oracle's
 view of the same inputs, and compare element by element.
 
-Tolerance for floating-point results, against the float64 oracle:
-max-abs error <= 2e-2 and relative L2 error <= 5e-3.
+Tolerance for floating-point results, against the float64 oracle: relative L2
+error <= 5e-3 and, per element, |got - want| <= max(2e-2, ulp_bf16(want)).
+The results are bf16 tensors. Where |want| >= 4 the spacing of bf16 values
+(one ulp) is >= 0.03125, so even the correctly rounded value can sit more than
+2e-2 away, and the path's two bf16 roundings (hidden activation, then output)
+can land one ulp away; there the bound is that one ulp. Below |want| = 2.56 the
+bound is the plain 2e-2.
 """
 from __future__ import annotations
 
@@ -18,6 +23,12 @@ MAX_ABS = 2e-2
 REL_L2 = 5e-3
 
 
+def bf16_ulp(x) -> np.ndarray:
+    """Spacing of bf16 values at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(ax)) - 7)
+
+
 def assert_close(got, want, what=""):
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
@@ -25,14 +36,18 @@ def assert_close(got, want, what=""):
     if got.size == 0:
         return
     err = np.abs(got - want)
-    mx = float(err.max())
+    bound = np.maximum(MAX_ABS, bf16_ulp(want))
+    worst = int(np.argmax(err / bound))
     den = float(np.linalg.norm(want))
     rel = float(np.linalg.norm(got - want)) / den if den > 0 else float(np.linalg.norm(got))
-    assert mx <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rel:.3e}"
+    assert err.flat[worst] <= bound.flat[worst] and rel <= REL_L2, (
+        f"{what}: max-abs {err.max():.3e}, worst {err.flat[worst]:.3e} at |want| "
+        f"{abs(want.flat[worst]):.3f} (bound {bound.flat[worst]:.3e}), rel-L2 {rel:.3e}")
 
 
 def f64(t: torch.Tensor) -> np.ndarray:
-    return t.detach().float().cpu().numpy().astype(np.float64)
+    """Exact float64 copy (bf16 and fp32 widen exactly; done on the tensor's device)."""
+    return t.detach().double().cpu().numpy()
 
 
 def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0):
@@ -172,18 +187,31 @@ def check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=None, rng=None
             v, r0 = int(plan.band_valid[o][b]), int(plan.band_dst_row[o][b])
             assert torch.equal(layer.recv[dst][r0:r0 + v], Y[b * wl.tb_M:b * wl.tb_M + v]), \
                 f"combine copy of band {b} of rank {o}"
-    # Scale: per token sum over its k experts.
-    for s in range(W):
-        toks = range(T) if sample is None else np.sort(rng.choice(T, size=min(sample, T), replace=False))
-        got = f64(layer.out[s][torch.as_tensor(np.asarray(list(toks)), device=layer.out[s].device)])
-        want = np.zeros_like(got)
-        for n, t in enumerate(toks):
+    # Scale: per token sum over its k experts, evaluated expert by expert.
+    picks = {}
+    for s_ in range(W):
+        toks = np.arange(T) if sample is None else np.sort(
+            rng.choice(T, size=min(sample, T), replace=False))
+        picks[s_] = toks
+    need = {}
+    for s_, toks in picks.items():
+        for t in toks.tolist():
             for j in range(wl.topk):
-                e = int(ids[s, t, j])
-                o, li = divmod(e, wl.L)
-                y = O.expert_ffn(xs[s][t][None], wg[o][li], wu[o][li], wd[o][li])[0]
-                want[n] += w[s, t, j] * y
-        assert_close(got, want, f"out rank {s}")
+                need.setdefault(int(ids[s_, t, j]), []).append((s_, t, j))
+    yv = {}
+    for e in sorted(need):
+        o, li = divmod(e, wl.L)
+        rows = np.stack([xs[s_][t] for s_, t, _ in need[e]])
+        ys = O.expert_ffn(rows, wg[o][li], wu[o][li], wd[o][li])
+        for key, y in zip(need[e], ys):
+            yv[key] = y
+    for s_, toks in picks.items():
+        got = f64(layer.out[s_][torch.as_tensor(toks, device=layer.out[s_].device)])
+        want = np.zeros_like(got)
+        for n, t in enumerate(toks.tolist()):
+            for j in range(wl.topk):
+                want[n] += w[s_, t, j] * yv[(s_, t, j)]
+        assert_close(got, want, f"out rank {s_}")
 
 
 class _LazyExperts:

@@ -85,9 +85,10 @@ def test_ffn_closed_form_and_operand_roles():
     x = np.array([[l3]])
     one, two = np.array([[1.0]]), np.array([[2.0]])
     # gate = x, up = 2x:  SiLU(ln3) * 2 ln3 = 1.5 (ln3)^2
-    np.testing.assert_allclose(O.expert_ffn(x, one, two, one), [[1.5 * l3 * l3]], rtol=1e-14)
+    ffn = lambda *a: O.expert_ffn(*a, round_hidden=False)
+    np.testing.assert_allclose(ffn(x, one, two, one), [[1.5 * l3 * l3]], rtol=1e-14)
     # gate and up swapped: SiLU(2 ln3) * ln3 = 2 ln3 * (9/10) * ln3 = 1.8 (ln3)^2
-    np.testing.assert_allclose(O.expert_ffn(x, two, one, one), [[1.8 * l3 * l3]], rtol=1e-14)
+    np.testing.assert_allclose(ffn(x, two, one, one), [[1.8 * l3 * l3]], rtol=1e-14)
     # rectangular operands in nn.Linear layout: D=2, F=3
     x = np.array([[l3, 0.0]])
     wg = np.array([[1.0, 5.0], [0.0, 1.0], [-1.0, 7.0]])  # g = (ln3, 0, -ln3)
@@ -95,12 +96,36 @@ def test_ffn_closed_form_and_operand_roles():
     wd = np.array([[1.0, 0.0, 0.0], [0.0, 0.0, 1.0]])     # y = (a0, a2)
     a0 = 0.75 * l3 * l3
     a2 = -0.25 * l3 * l3
-    np.testing.assert_allclose(O.expert_ffn(x, wg, wu, wd), [[a0, a2]], rtol=1e-14)
+    np.testing.assert_allclose(ffn(x, wg, wu, wd), [[a0, a2]], rtol=1e-14)
     # zero input gives zero output; output is linear in W_down
     assert not O.expert_ffn(np.zeros((2, 2)), wg, wu, wd).any()
     rng = np.random.default_rng(0)
     xr = rng.standard_normal((4, 2))
     np.testing.assert_allclose(O.expert_ffn(xr, wg, wu, 3 * wd), 3 * O.expert_ffn(xr, wg, wu, wd))
+
+
+def test_round_bf16_matches_the_library_conversion():
+    """round_bf16 against torch's float32 -> bfloat16 conversion (round to nearest even)."""
+    import torch
+    rng = np.random.default_rng(11)
+    v = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-6, 6, 4000),
+                        [0.0, -0.0, 1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -9,
+                         3.0 * 2.0 ** 100, -65504.0]])
+    want = torch.tensor(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(O.round_bf16(v.astype(np.float32)), want)
+    assert O.round_bf16(1.0 + 2.0 ** -8) == 1.0            # tie -> even (mantissa 0)
+    assert O.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6  # tie -> even (up)
+
+
+def test_ffn_rounds_the_hidden_activation():
+    # x = 2, all weights 1: g = u = 2, h = 2 * 2 * sigma(2) = 3.5232..., bf16 -> 3.515625
+    x = np.array([[2.0]])
+    one = np.array([[1.0]])
+    h = 4.0 / (1.0 + np.exp(-2.0))
+    assert abs(h - 3.52318831) < 1e-8
+    assert O.expert_ffn(x, one, one, one)[0, 0] == 3.515625
+    assert O.expert_ffn(x, one, one, 2 * one)[0, 0] == 7.03125
+    np.testing.assert_allclose(O.expert_ffn(x, one, one, one, round_hidden=False), [[h]], rtol=1e-15)
 
 
 # ---------------------------------------------------------------- layout / schedule / plan
@@ -310,6 +335,7 @@ def _direct(x, ids, w, wg, wu, wd, L):
                 g = wg[o][li].astype(np.float64) @ xv
                 u = wu[o][li].astype(np.float64) @ xv
                 a = np.array([gi / (1.0 + math.exp(-gi)) for gi in g]) * u
+                a = O.round_bf16(a)  # the second GEMM's operand is bf16
                 out[s][t] += w[s, t, j] * (wd[o][li].astype(np.float64) @ a)
     return out
 
@@ -386,3 +412,11 @@ def test_receive_order_example():
     assert p.recv_rows.tolist() == g["recv_rows"]
     assert p.src[0].tolist() == g["scale_map_rank0"]
     _check_invariants(np.array(g["ids"]), p)
+
+
+def test_bf16_ulp_helper_used_by_the_gpu_tolerance():
+    """The element bound of the GPU parity tests: bf16 spacing at a few exact points."""
+    from tests.parity import bf16_ulp
+    assert bf16_ulp(1.0) == 2.0 ** -7 and bf16_ulp(1.99) == 2.0 ** -7
+    assert bf16_ulp(4.0) == 2.0 ** -5 and bf16_ulp(-8.5) == 2.0 ** -4
+    assert bf16_ulp(2.56) == 2.0 ** -6 < 2e-2 < bf16_ulp(4.0)
