@@ -45,8 +45,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, index):
+        self.index = index  # physical index or "GPU-<uuid>"
         self.proc = None
         self.file = None
 
@@ -92,6 +92,23 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def max_over_ranks(v: float, device="cpu") -> float:
+    """Largest value over the ranks of the default process group (v itself alone)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_replica: int, ms_step_max: float) -> float:
+    """Whole-job throughput: every replica's tokens over the slowest replica's step."""
+    return world * tokens_per_replica / (ms_step_max * 1e-3)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def gpu_arm(args, rank, world, local_rank):
@@ -103,6 +120,8 @@ def gpu_arm(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     wl = get_workload(args.workload)
+    if args.tokens_per_rank:
+        wl = get_workload(args.workload, T=args.tokens_per_rank)
     W, T, D, F, k = wl.W, wl.T, wl.d_model, wl.d_ff, wl.topk
     inp = make_inputs(wl, device="cuda")
     layer = ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas)
@@ -129,46 +148,31 @@ def gpu_arm(args, rank, world, local_rank):
     flops_valid = 6.0 * valid_rows * D * F
 
     # ---- timed region: K steps, inputs resident in HBM ------------------------------
+    # The library records CUDA events around each of its kernels on the kernel's own
+    # stream (no host synchronisation inside the region); their means give the
+    # producer's launch time for the roofline.
     layer.set_timing(True)
-    prod_ms, cons_ms = [], []
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    with ClockSampler(gpu_id) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         t_wall = time.perf_counter()
         ev0.record(sp)
         for _ in range(args.steps):
             step()
-            t = layer.timings()  # waits for this step's events (one step in flight)
-            prod_ms.append(t[2])
-            cons_ms.append(t[3])
         ev1.record(sp)
         torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
         wall = time.perf_counter() - t_wall
-    if world > 1:
-        torch.distributed.barrier()
-    ms_total = ev0.elapsed_time(ev1)
+    kernel_ms = layer.timings()
     layer.set_timing(False)
-
-    # The per-step event read above serialises steps on the host; time the same K steps
-    # again back to back without reading timings, and take that as the step time.
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ev0.record(sp)
-    for _ in range(args.steps):
-        step()
-    ev1.record(sp)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ms_free = ev0.elapsed_time(ev1)
-    ms_step = ms_free / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, device="cuda")
     code, detail = layer.status()
     if code != 0:
         raise RuntimeError(f"device status {code} detail {detail} after the timed region")
@@ -180,11 +184,11 @@ def gpu_arm(args, rank, world, local_rank):
     e2e = e2e_arm(layer, inp, wl, sp, sc, args)
 
     hbm, bf16, bf16_sus, src = _peaks()
-    prod_avg = statistics.mean(prod_ms)
+    prod_avg = kernel_ms[2]
     achieved = flops_exec / (prod_avg * 1e-3) / 1e12
     result = {
         "metric": METRIC,
-        "value": world * W * T / (ms_step * 1e-3),
+        "value": job_tokens_per_s(world, W * T, ms_step),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -213,7 +217,8 @@ def gpu_arm(args, rank, world, local_rank):
                  "tflop_executed": flops_exec / 1e12, "tflop_valid": flops_valid / 1e12,
                  "recv_rows": recv_rows},
         "timed_wall_s": wall,
-        "timed_event_ms": ms_total,
+        "kernel_ms_in_timed_region": dict(zip(
+            ["route", "plan", "producer", "consumer", "scale", "gather"], kernel_ms)),
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
@@ -391,11 +396,15 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--consumer-ctas", type=int, default=8)
+    ap.add_argument("--consumer-ctas", type=int, default=8,
+                    help="consumer CTAs beside the producer; 0 runs the two kernels serially "
+                         "(needed under a profiler, which serialises kernel launches)")
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

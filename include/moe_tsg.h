@@ -189,11 +189,13 @@ enum moe_field {
 };
 int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count);
 
-/* Elapsed device time in ms of the kernels enqueued by the last calls, measured
- * with CUDA events recorded on the stream each kernel ran on. Synchronises on the
+/* Device time in ms of the kernels the calls enqueue, measured with CUDA events
+ * recorded on the stream each kernel ran on: the mean over the calls made since
+ * timing was last enabled (the most recent 64 of them). Synchronises on those
  * events. Order: [0] route, [1] plan (all plan kernels and the gather),
  * [2] producer, [3] consumer, [4] scale, [5] gather only. A slot with no
- * measurement is -1. Pure instrumentation; records events only when enabled. */
+ * measurement is -1. Instrumentation only: events are recorded only while
+ * enabled, and enabling resets the counts. */
 int moe_set_timing(moe_plan *plan, int enable);
 int moe_timings(moe_plan *plan, float *ms, int n);
 

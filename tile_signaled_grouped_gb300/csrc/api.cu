@@ -18,6 +18,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 enum TimingSlot { kTRoute = 0, kTPlan, kTProducer, kTConsumer, kTScale, kTGather, kTSlots };
+constexpr int kTRing = 64;  // event pairs kept per timing slot
 
 }  // namespace
 
@@ -32,8 +33,8 @@ struct moe_plan {
   int num_sms;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   cudaEvent_t ev_ready, ev_join;
-  cudaEvent_t ev_t0[kTSlots], ev_t1[kTSlots];
-  bool recorded[kTSlots];
+  cudaEvent_t ev_t0[kTSlots][kTRing], ev_t1[kTSlots][kTRing];
+  int nrec[kTSlots];  // measurements recorded since timing was enabled
   bool timing;
 };
 
@@ -46,7 +47,7 @@ int dims_from_cfg(const moe_cfg* c, Dims* d) {
   if (E > 1024 || c->topk < 1 || c->topk > std::min<long long>(E, 32)) return MOE_ERR_ARG;
   if (c->T < 1 || c->T > (1 << 20)) return MOE_ERR_ARG;
   if (c->d_model < 128 || c->d_model % 128 || c->d_ff < 128 || c->d_ff % 128) return MOE_ERR_ARG;
-  if (c->d_model > 65536 || c->d_ff > 65536) return MOE_ERR_ARG;
+  if (c->d_model > 16384 || c->d_ff > 65536) return MOE_ERR_UNSUPPORTED;  // a row fits one copy chunk
   if (c->tb_M != 64 && c->tb_M != 128 && c->tb_M != 256) return MOE_ERR_ARG;
   if (c->mgb < 1 || c->consumer_ctas < 0) return MOE_ERR_ARG;
   Dims x{};
@@ -73,6 +74,10 @@ int dims_from_cfg(const moe_cfg* c, Dims* d) {
   x.N2 = x.D % 256 == 0 ? 256 : 128;
   x.nt1 = x.F / kN1;
   x.nt2 = x.D / x.N2;
+  x.rpc = std::max(1, kChunkBytes / (x.D * 2));
+  // A segment spans at most mgb bands of tb rows; it must split into at most
+  // kMaxSegChunks copy chunks.
+  if (((long long)c->mgb * c->tb_M + x.rpc - 1) / x.rpc > kMaxSegChunks) return MOE_ERR_UNSUPPORTED;
   *d = x;
   return MOE_OK;
 }
@@ -92,7 +97,6 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_CNT] = n[PA_GROUP_START] = n[PA_RECV_OFF] = E * W;
   n[PA_EXPERT_START] = n[PA_ROWS_ALLOC] = n[PA_NB] = n[PA_NRB] = E;
   n[PA_RANK_ROWS] = n[PA_RANK_NB] = n[PA_RANK_NREMOTE] = n[PA_RECV_ROWS] = n[PA_RANK_NSEG] = W;
-  n[PA_RANK_NMT] = n[PA_RANK_NMT_REMOTE] = W;
   n[PA_BAND_EXPERT] = n[PA_BAND_DST] = n[PA_BAND_VALID] = n[PA_BAND_DST_ROW] = W * NBM;
   n[PA_BAND_TILE] = W * NBM;
   n[PA_SCHED] = n[PA_SEG_FIRST] = n[PA_SEG_NB] = n[PA_SEG_GIDX] = W * NBM;
@@ -101,6 +105,8 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_TILE_ROW] = n[PA_TILE_EXPERT] = W * NMM;
   n[PA_UNIT_BEGIN] = W * (NMM / kTileGroup + 2) + 1;
   n[PA_SEG_ORDER] = W * NBM;
+  n[PA_SEG_REC] = W * NBM * kSegRec;
+  n[PA_GROUP_NCHUNK] = W * W;
   n[PA_XSRC] = W * (size_t)d.RM;
   n[PA_SCALE_SRC] = W * (size_t)d.T * d.k;
   size_t pos = 0;
@@ -146,12 +152,12 @@ DevPlan dev_plan(const moe_plan* p) {
 bool aligned16(const void* ptr) { return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
 void tstart(moe_plan* p, int slot, cudaStream_t s) {
-  if (p->timing) cudaEventRecord(p->ev_t0[slot], s);
+  if (p->timing) cudaEventRecord(p->ev_t0[slot][p->nrec[slot] % kTRing], s);
 }
 void tstop(moe_plan* p, int slot, cudaStream_t s) {
   if (p->timing) {
-    cudaEventRecord(p->ev_t1[slot], s);
-    p->recorded[slot] = true;
+    cudaEventRecord(p->ev_t1[slot][p->nrec[slot] % kTRing], s);
+    p->nrec[slot]++;
   }
 }
 
@@ -232,6 +238,10 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
     return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;
 
+  if (preload_producer() != cudaSuccess || preload_consumer() != cudaSuccess ||
+      preload_plan() != cudaSuccess || preload_route_scale() != cudaSuccess)
+    return MOE_ERR_CUDA;
+
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
@@ -253,7 +263,9 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
   bool ok = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; i < kTSlots && ok; ++i)
-    ok = cudaEventCreate(&p->ev_t0[i]) == cudaSuccess && cudaEventCreate(&p->ev_t1[i]) == cudaSuccess;
+    for (int j = 0; j < kTRing && ok; ++j)
+      ok = cudaEventCreate(&p->ev_t0[i][j]) == cudaSuccess &&
+           cudaEventCreate(&p->ev_t1[i][j]) == cudaSuccess;
   if (!ok) {
     moe_plan_destroy(p);
     return MOE_ERR_CUDA;
@@ -267,10 +279,11 @@ void moe_plan_destroy(moe_plan* p) {
   if (p == nullptr) return;
   if (p->ev_ready) cudaEventDestroy(p->ev_ready);
   if (p->ev_join) cudaEventDestroy(p->ev_join);
-  for (int i = 0; i < kTSlots; ++i) {
-    if (p->ev_t0[i]) cudaEventDestroy(p->ev_t0[i]);
-    if (p->ev_t1[i]) cudaEventDestroy(p->ev_t1[i]);
-  }
+  for (int i = 0; i < kTSlots; ++i)
+    for (int j = 0; j < kTRing; ++j) {
+      if (p->ev_t0[i][j]) cudaEventDestroy(p->ev_t0[i][j]);
+      if (p->ev_t1[i][j]) cudaEventDestroy(p->ev_t1[i][j]);
+    }
   delete p;
 }
 
@@ -349,8 +362,6 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
     ca.y[r] = pa.y[r];
     ca.recv[r] = static_cast<__nv_bfloat16*>(recv[r]);
   }
-  const int groups = std::max(1, d.W * (d.W - 1));
-  ca.parts_per_group = std::max(1, (cgrid + groups - 1) / groups);
 
   // Ready flags, GEMM1 counters, the ticket counter and the group signals start at 0.
   const size_t z0 = p->offsets[PA_QUEUE];
@@ -419,7 +430,7 @@ int moe_status_clear(moe_plan* p, moe_stream_t stream) {
 int moe_set_timing(moe_plan* p, int enable) {
   if (p == nullptr) return MOE_ERR_ARG;
   p->timing = enable != 0;
-  for (int i = 0; i < kTSlots; ++i) p->recorded[i] = false;
+  for (int i = 0; i < kTSlots; ++i) p->nrec[i] = 0;
   return MOE_OK;
 }
 
@@ -427,11 +438,17 @@ int moe_timings(moe_plan* p, float* ms, int n) {
   if (p == nullptr || ms == nullptr) return MOE_ERR_ARG;
   for (int i = 0; i < n; ++i) {
     ms[i] = -1.f;
-    if (i >= kTSlots || !p->recorded[i]) continue;
-    CUDA_TRY(cudaEventSynchronize(p->ev_t1[i]));
-    float v = 0.f;
-    CUDA_TRY(cudaEventElapsedTime(&v, p->ev_t0[i], p->ev_t1[i]));
-    ms[i] = v;
+    if (i >= kTSlots || p->nrec[i] == 0) continue;
+    const int m = std::min(p->nrec[i], kTRing);
+    double sum = 0.0;
+    for (int j = 0; j < m; ++j) {
+      const int q = (p->nrec[i] - 1 - j) % kTRing;
+      CUDA_TRY(cudaEventSynchronize(p->ev_t1[i][q]));
+      float v = 0.f;
+      CUDA_TRY(cudaEventElapsedTime(&v, p->ev_t0[i][q], p->ev_t1[i][q]));
+      sum += v;
+    }
+    ms[i] = (float)(sum / m);
   }
   return MOE_OK;
 }

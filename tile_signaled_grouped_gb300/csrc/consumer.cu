@@ -7,121 +7,252 @@
 // the producer only through device memory; section 4.5: destination, offset and
 // valid-row count come from the precomputed combine plan (padding is never sent).
 // Perseus summary (papercache.org), section 4.1, Algorithm 1: data moves without
-// signals, then ONE fence per destination group precedes that group's signal.
+// signals; one fence then precedes the signals of a whole destination group.
 //
-// Here a group is (sender rank o, destination rank s). Its segments are split
-// into `parts_per_group` parts (segment index modulo parts); a part is owned by
-// one CTA, which copies the part's segments in the producer's tile order, then
-// issues a single release (bar.sync + fence + atomic) for the whole part. The
-// CTA that completes a group's last part stores the group signal. With one part
-// per group this is exactly one fence per destination group.
+// GB300 form: each segment is cut into chunks of rpc rows (up to 40 KB); the
+// chunks of all segments, in the producer's tile order, are dealt round-robin to
+// the consumer CTAs, so every CTA follows production and the last segment is
+// copied by all of them. A CTA is one warp: the lanes poll the flags of a chunk's
+// bands together, and lane 0 moves the chunk with TMA bulk copies through a
+// three-slot shared-memory ring (global -> shared completes on an mbarrier,
+// shared -> global as a bulk group). A group is (sender o, destination s). When a
+// CTA has stored the last of its chunks of a group it waits for those stores,
+// issues one fence and one release increment of the group's chunk count; the
+// increment that completes the group stores the group signal.
 #include "moe_common.cuh"
 
 namespace moe {
 namespace {
 
+constexpr int kMaxGroups = MOE_MAX_RANKS * MOE_MAX_RANKS;
+
+constexpr int kListCap = kMaxSegChunks;  // owned chunks listed per batch of records
+
+struct ConsumerSmem {
+  uint64_t full[kChunkSlots];
+  int owned[kMaxGroups];  // this CTA's chunks of each group not yet stored
+  int total[kMaxGroups];  // this CTA's chunks of each group
+  int rec[32][kSegRec];   // a batch of segment records
+  int list[kListCap];     // owned chunks of the batch: (record << 24) | chunk index
+};
+
+static_assert(sizeof(ConsumerSmem) <= kConsumerSmemTail, "consumer shared memory layout");
+
+// Chunks i in [cb, cb + n) with i % G == c.
+__device__ __forceinline__ int owned_count(int cb, int n, int c, int G) {
+  const int i0 = cb + ((c - cb) % G + G) % G;
+  return i0 >= cb + n ? 0 : (cb + n - 1 - i0) / G + 1;
+}
+
 __global__ void __launch_bounds__(kConsumerThreads, 1)
     consumer_kernel(const __grid_constant__ ConsumerArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* slots = smem_raw;
+  ConsumerSmem& sm = *reinterpret_cast<ConsumerSmem*>(smem_raw + (size_t)kChunkSlots * kChunkBytes);
   const Dims d = a.p.d;
   uint32_t* status = reinterpret_cast<uint32_t*>(a.p.a[PA_STATUS]);
   const uint32_t* flags = reinterpret_cast<const uint32_t*>(a.p.a[PA_FLAGS]);
   uint32_t* group_done = reinterpret_cast<uint32_t*>(a.p.a[PA_GROUP_DONE]);
   uint32_t* group_sig = reinterpret_cast<uint32_t*>(a.p.a[PA_GROUP_SIG]);
-  const int32_t* order = a.p.a[PA_SEG_ORDER];
-  const int R = a.parts_per_group;
+  const int32_t* recs = a.p.a[PA_SEG_REC];
+  const int32_t* gchunks = a.p.a[PA_GROUP_NCHUNK];
   const int nseg = a.p.a[PA_TOTALS][1];
-  const int tid = threadIdx.x, lane = tid & 31;
-  __shared__ int s_go;
+  const int lane = threadIdx.x;
+  const int c = blockIdx.x, G = gridDim.x;
+  const size_t row_bytes = (size_t)d.D * 2;
 
-  for (int idx = 0; idx < nseg; ++idx) {
-    const int code = order[idx];
-    const int o = code / d.NBM, j = code % d.NBM;
-    const size_t rb = (size_t)o * d.NBM;
-    const int gidx = a.p.a[PA_SEG_GIDX][rb + j];
-    const int first = a.p.a[PA_SEG_FIRST][rb + j];
-    const int nbands = a.p.a[PA_SEG_NB][rb + j];
-    const int b0 = a.p.a[PA_SCHED][rb + first];
-    const int dst = a.p.a[PA_BAND_DST][rb + b0];
-    const int g = o * d.W + dst;
-    const int part = g * R + gidx % R;
-    if (part % (int)gridDim.x != (int)blockIdx.x) continue;
+  for (int g = lane; g < kMaxGroups; g += 32) sm.owned[g] = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kChunkSlots; ++i) mbar_init(&sm.full[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  // Pre-pass: how many chunks of each group this CTA copies.
+  for (int idx = lane; idx < nseg; idx += 32) {
+    const int32_t* r = recs + (size_t)idx * kSegRec;
+    const int n = owned_count(r[6], r[7], c, G);
+    if (n) atomicAdd(&sm.owned[r[0] * d.W + r[1]], n);
+  }
+  __syncwarp();
+  for (int g = lane; g < kMaxGroups; g += 32) sm.total[g] = sm.owned[g];
+  __syncwarp();
 
-    // Wait (bounded) until every tile of every band of the segment is flagged.
-    if (tid < 32) {
-      bool ok = true;
-      const unsigned long long t0 = globaltimer();
-      for (int b = b0; b < b0 + nbands && ok; ++b) {
-        const uint32_t* f = flags + (rb + b) * d.nt2;
-        for (int c = lane; c < d.nt2 && ok; c += 32) {
-          while (ld_acquire_u32(f + c) < (uint32_t)d.parts) {
-            if (ld_relaxed_u32(status) != 0) {
-              ok = false;
-              break;
+  // Copy pipeline, driven by lane 0. Chunk i (in this CTA's order) uses slot i % S
+  // and completes phase (i / S) & 1 of that slot's barrier. At most two loads are
+  // outstanding; a slot is refilled only after the store that last used it has
+  // finished reading it.
+  struct Pend {
+    uint8_t* dst;
+    uint32_t bytes;
+    int group;
+  };
+  Pend pend[kChunkSlots] = {};
+  int n = 0, stored = 0;
+  bool ok = true;
+  const long long itimeout = a.p.timeout_ns + 4000000000LL;
+
+  auto store_next = [&]() {  // lane 0: store chunk `stored` once its load has landed
+    const int slot = stored % kChunkSlots;
+    volatile int never = 0;
+    if (!mbar_wait_bounded(&sm.full[slot], (stored / kChunkSlots) & 1, &never, itimeout, status,
+                           0x60000000u))
+      ok = false;
+    bulk_store(pend[slot].dst, slots + (size_t)slot * kChunkBytes, pend[slot].bytes);
+    bulk_commit();
+    ++stored;
+    const int g = pend[slot].group;
+    if (--sm.owned[g] == 0) {
+      // This CTA's last chunk of group g: one fence for all of them, then the count.
+      bulk_wait_all();
+      fence_proxy_async_global();
+      fence_acq_rel_gpu();
+      const uint32_t mine = (uint32_t)sm.total[g];
+      const uint32_t done = atomicAdd(group_done + g, mine) + mine;
+      if (done == (uint32_t)gchunks[g]) st_release_u32(group_sig + g, 1u);
+    }
+  };
+
+  // Rows and flags of listed chunk `e` (a packed list entry).
+  auto chunk_of = [&](int e, int& q, int& r0, int& r1) {
+    q = e >> 24;
+    const int k = e & 0xFFFFFF;
+    r0 = k * d.rpc;
+    r1 = min(sm.rec[q][4], r0 + d.rpc);
+  };
+  auto flags_ready = [&](int q, int r0, int r1, int lane_lo, int lane_step) {
+    const int b0 = sm.rec[q][2];
+    const size_t rb = (size_t)sm.rec[q][0] * d.NBM;
+    const int bl = b0 + r0 / d.tb, bh = b0 + (r1 - 1) / d.tb;
+    const uint32_t* f = flags + (rb + bl) * d.nt2;
+    const int nflags = (bh - bl + 1) * d.nt2;
+    bool ready = true;
+    for (int i = lane_lo; i < nflags; i += lane_step) ready &= ld_acquire_u32(f + i) >= (uint32_t)d.parts;
+    return ready;
+  };
+
+  int base = 0;
+  while (base < nseg && ok) {
+    // Load up to 32 records and list this CTA's chunks of as many of them as fit.
+    const int nb = min(32, nseg - base);
+    __syncwarp();
+    int cnt = 0;
+    if (lane < nb) {
+      const int32_t* r = recs + (size_t)(base + lane) * kSegRec;
+#pragma unroll
+      for (int q = 0; q < kSegRec; ++q) sm.rec[lane][q] = r[q];
+      cnt = owned_count(r[6], r[7], c, G);
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    // Records taken: every lane whose inclusive count fits (the first always fits,
+    // because a segment has at most kListCap chunks).
+    const unsigned fit = __ballot_sync(0xffffffffu, lane < nb && incl <= kListCap);
+    const int take = max(1, __popc(fit));
+    const int nlist = __shfl_sync(0xffffffffu, incl, take - 1);
+    if (lane < take && cnt > 0) {
+      const int cb = sm.rec[lane][6];
+      int k = ((c - cb) % G + G) % G;
+      for (int j = 0, pos = incl - cnt; j < cnt; ++j, ++pos, k += G) sm.list[pos] = (lane << 24) | k;
+    }
+    __syncwarp();
+
+    // Walk the listed chunks 32 at a time: every lane checks one chunk's flags, so
+    // the flag latency is paid once per 32 chunks while copies are in flight.
+    for (int s0 = 0; s0 < nlist && ok; s0 += 32) {
+      const int m = min(32, nlist - s0);
+      bool mine = true;
+      if (lane < m) {
+        int q, r0, r1;
+        chunk_of(sm.list[s0 + lane], q, r0, r1);
+        mine = flags_ready(q, r0, r1, 0, 1);
+      }
+      unsigned ready = __ballot_sync(0xffffffffu, mine);
+      for (int j = 0; j < m && ok; ++j) {
+        int q, r0, r1;
+        chunk_of(sm.list[s0 + j], q, r0, r1);
+        if (!(ready >> j & 1u)) {
+          // Not produced yet: store everything loaded, then wait (bounded, all lanes).
+          if (lane == 0)
+            while (stored < n) store_next();
+          const unsigned long long t0 = globaltimer();
+          bool done = false, stop = false;
+          while (!done && !stop) {
+            done = __all_sync(0xffffffffu, flags_ready(q, r0, r1, lane, 32));
+            if (!done) {
+              __nanosleep(64);
+              if (lane == 0) {
+                if (ld_relaxed_u32(status) != 0) {
+                  stop = true;
+                } else if ((long long)(globaltimer() - t0) > a.p.timeout_ns) {
+                  const int bl = sm.rec[q][2] + r0 / d.tb;
+                  report_error(status, MOE_DEV_TIMEOUT,
+                               0x50000000u | (uint32_t)((size_t)sm.rec[q][0] * d.NBM + bl));
+                  stop = true;
+                }
+              }
+              stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
             }
-            if ((long long)(globaltimer() - t0) > a.p.timeout_ns) {
-              report_error(status, MOE_DEV_TIMEOUT, 0x50000000u | (uint32_t)(rb + b));
-              ok = false;
-              break;
-            }
-            __nanosleep(32);
           }
+          if (stop) {
+            ok = false;
+            break;
+          }
+          // Chunks after this one may have become ready meanwhile.
+          bool again = true;
+          if (lane > j && lane < m) {
+            int q2, a0, a1;
+            chunk_of(sm.list[s0 + lane], q2, a0, a1);
+            again = flags_ready(q2, a0, a1, 0, 1);
+          }
+          ready = __ballot_sync(0xffffffffu, again) | ((1u << j) << 1) - 1u;
         }
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      if (lane == 0) s_go = ok;
-    }
-    __syncthreads();
-    if (!s_go) return;  // an error is recorded; nothing waits on this CTA
-
-    // Valid rows of the segment are contiguous: only a group's last band is partial.
-    const int vrows = (nbands - 1) * d.tb + a.p.a[PA_BAND_VALID][rb + b0 + nbands - 1];
-    const int drow = a.p.a[PA_BAND_DST_ROW][rb + b0];
-    const uint4* src = reinterpret_cast<const uint4*>(a.y[o] + (size_t)b0 * d.tb * d.D);
-    uint4* out = reinterpret_cast<uint4*>(a.recv[dst] + (size_t)drow * d.D);
-    const long long n16 = (long long)vrows * d.D / 8;
-    long long i = tid;
-    for (; i + 3LL * kConsumerThreads < n16; i += 4LL * kConsumerThreads) {
-      const uint4 v0 = __ldcg(src + i);
-      const uint4 v1 = __ldcg(src + i + kConsumerThreads);
-      const uint4 v2 = __ldcg(src + i + 2 * kConsumerThreads);
-      const uint4 v3 = __ldcg(src + i + 3 * kConsumerThreads);
-      __stcg(out + i, v0);
-      __stcg(out + i + kConsumerThreads, v1);
-      __stcg(out + i + 2 * kConsumerThreads, v2);
-      __stcg(out + i + 3 * kConsumerThreads, v3);
-    }
-    for (; i < n16; i += kConsumerThreads) __stcg(out + i, __ldcg(src + i));
-
-    // Last segment of this part: one release for the part, and the group signal
-    // from whoever completes the group.
-    const int gn = a.p.a[PA_GROUP_NSEG][o * d.W + dst];
-    if (gidx + R >= gn) {
-      __syncthreads();
-      if (tid == 0) {
-        fence_acq_rel_gpu();
-        const uint32_t done = atomicAdd(group_done + g, 1u) + 1u;
-        if (done == (uint32_t)min(R, gn)) {
-          fence_acq_rel_gpu();
-          st_release_u32(group_sig + g, 1u);
+        if (lane == 0) {
+          fence_proxy_async_global();  // the flags were acquired; the bulk load reads Y
+          if (n - stored == kChunkSlots) store_next();
+          if (n >= kChunkSlots) bulk_wait_read<0>();  // the slot's last store has read it
+          const int o = sm.rec[q][0], dst = sm.rec[q][1], b0 = sm.rec[q][2];
+          const int slot = n % kChunkSlots;
+          const uint32_t bytes = (uint32_t)((size_t)(r1 - r0) * row_bytes);
+          const uint8_t* src =
+              reinterpret_cast<const uint8_t*>(a.y[o]) + ((size_t)b0 * d.tb + r0) * row_bytes;
+          pend[slot].dst =
+              reinterpret_cast<uint8_t*>(a.recv[dst]) + ((size_t)sm.rec[q][5] + r0) * row_bytes;
+          pend[slot].bytes = bytes;
+          pend[slot].group = o * d.W + dst;
+          mbar_arrive_expect_tx(&sm.full[slot], bytes);
+          bulk_load(slots + (size_t)slot * kChunkBytes, src, bytes, &sm.full[slot]);
+          ++n;
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
     }
-    __syncthreads();  // s_go is rewritten by the next segment
+    base += take;
+  }
+  if (lane == 0) {
+    // Drain: store what was loaded (even after an error, so no copy outlives the
+    // CTA's shared memory), then wait for every store.
+    while (stored < n) store_next();
+    bulk_wait_all();
   }
 }
 
 }  // namespace
 
+cudaError_t preload_consumer() {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, consumer_kernel);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(consumer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kConsumerSmem);
+}
+
 cudaError_t launch_consumer(const ConsumerArgs& a, int grid, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(consumer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kConsumerSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  // The dynamic shared memory is reserved, not used: it keeps a consumer CTA from
-  // sharing an SM with a producer CTA, so the two kernels run on disjoint SMs.
+  // 120 KB of shared memory per CTA also keeps a consumer CTA from sharing an SM
+  // with a producer CTA or another consumer CTA: the kernels run on disjoint SMs.
   consumer_kernel<<<grid, kConsumerThreads, kConsumerSmem, s>>>(a);
   return cudaGetLastError();
 }

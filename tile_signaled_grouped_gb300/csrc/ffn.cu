@@ -393,17 +393,15 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
 
 }  // namespace
 
-size_t producer_smem_bytes() { return kSmemBytes; }
+cudaError_t preload_producer() {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, ffn_producer_kernel);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(ffn_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmemBytes);
+}
 
 cudaError_t launch_producer(const ProducerArgs& a, int grid, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_producer_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   ffn_producer_kernel<<<grid, kProducerThreads, kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }

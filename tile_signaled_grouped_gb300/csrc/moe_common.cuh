@@ -22,8 +22,13 @@ constexpr int kStages = 4;       // shared-memory pipeline depth
 constexpr int kTaskRing = 4;     // task descriptors in flight inside one CTA
 constexpr int kTileGroup = 8;    // tiles per scheduling unit (weight reuse in L2)
 constexpr int kProducerThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kConsumerThreads = 512;
-constexpr size_t kConsumerSmem = 120 * 1024;  // keeps one consumer CTA alone on its SM
+constexpr int kConsumerThreads = 32;         // one warp: lane 0 drives the bulk copies
+constexpr int kChunkBytes = 40 * 1024;       // consumer copy chunk (one shared-memory slot)
+constexpr int kChunkSlots = 3;               // 120 KB: keeps one consumer CTA alone on its SM
+constexpr size_t kConsumerSmemTail = 4096;  // barriers, counters and records after the slots
+constexpr size_t kConsumerSmem = (size_t)kChunkSlots * kChunkBytes + kConsumerSmemTail;
+constexpr int kSegRec = 8;                   // ints per consumer segment record
+constexpr int kMaxSegChunks = 256;           // copy chunks one segment may have
 
 // ---------------------------------------------------------------------------
 // Dimensions derived from a configuration (host and device).
@@ -37,6 +42,7 @@ struct Dims {
   int N2;        // GEMM2 output columns per tile (256 or 128)
   int nt1, nt2;  // tiles along F (GEMM1) and along D (GEMM2)
   int parts;     // producer tiles touching one band (tb/128, at least 1)
+  int rpc;       // rows per consumer copy chunk
 };
 
 // Fields of the plan workspace, in placement order. The public moe_field enum
@@ -51,10 +57,10 @@ enum PlanArray {
   PA_WPRE, PA_CNT, PA_GROUP_START, PA_RECV_OFF,
   PA_EXPERT_START, PA_ROWS_ALLOC, PA_NB, PA_NRB,
   PA_RANK_ROWS, PA_RANK_NB, PA_RANK_NREMOTE, PA_RECV_ROWS, PA_RANK_NSEG,
-  PA_RANK_NMT, PA_RANK_NMT_REMOTE,
   PA_BAND_EXPERT, PA_BAND_DST, PA_BAND_VALID, PA_BAND_DST_ROW, PA_BAND_TILE,
   PA_SCHED, PA_SEG_FIRST, PA_SEG_NB, PA_SEG_GIDX, PA_GROUP_NSEG,
   PA_RANK_TILES, PA_TILE_ROW, PA_TILE_EXPERT, PA_UNIT_BEGIN, PA_SEG_ORDER,
+  PA_SEG_REC, PA_GROUP_NCHUNK,
   PA_XSRC, PA_SCALE_SRC,
   PA_COUNT
 };
@@ -84,6 +90,14 @@ struct DevPlan {
 // ---------------------------------------------------------------------------
 // Launchers (defined next to their kernels).
 // ---------------------------------------------------------------------------
+// Loads every kernel's module and sets its shared-memory limit. With lazy module
+// loading, the first launch of a kernel may wait for kernels already running; the
+// producer's first launch would then wait for a consumer that spins on the
+// producer's flags. Plan creation therefore loads all kernels up front.
+cudaError_t preload_producer();
+cudaError_t preload_consumer();
+cudaError_t preload_plan();
+cudaError_t preload_route_scale();
 cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* forced,
                          int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s);
@@ -107,7 +121,6 @@ struct ConsumerArgs {
   const __nv_bfloat16* y[MOE_MAX_RANKS];
   __nv_bfloat16* recv[MOE_MAX_RANKS];
   DevPlan p;
-  int parts_per_group;  // consumer parts each (sender, destination) group is split into
 };
 cudaError_t launch_consumer(const ConsumerArgs& a, int grid, cudaStream_t s);
 
@@ -216,6 +229,30 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+// Untiled bulk copies (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src_smem)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

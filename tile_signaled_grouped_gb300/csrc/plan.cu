@@ -483,8 +483,48 @@ __global__ void __launch_bounds__(1024) plan_order_kernel(DevPlan p) {
     if (v >= 0) p.a[PA_SEG_ORDER][idx] = v;
     carry += tot;
   }
+  const int nsegs = carry;
+  for (int g = tid; g < W * W; g += nt) p.a[PA_GROUP_NCHUNK][g] = 0;
+  __syncthreads();
+
+  // 4. One record per segment in consumer order: source band, destination, rows,
+  // and its range of copy chunks (rpc rows each) in the global chunk sequence.
+  int chunk_carry = 0;
+  for (int base = 0; base < nsegs; base += nt) {
+    const int idx = base + tid;
+    int nch = 0;
+    int rec[kSegRec] = {};
+    if (idx < nsegs) {
+      const int code = p.a[PA_SEG_ORDER][idx];
+      const int o = code / d.NBM, j = code % d.NBM;
+      const size_t rb = (size_t)o * d.NBM;
+      const int nb = p.a[PA_SEG_NB][rb + j];
+      const int b0 = p.a[PA_SCHED][rb + p.a[PA_SEG_FIRST][rb + j]];
+      const int dst = p.a[PA_BAND_DST][rb + b0];
+      const int vrows = (nb - 1) * tb + p.a[PA_BAND_VALID][rb + b0 + nb - 1];
+      nch = (vrows + d.rpc - 1) / d.rpc;
+      rec[0] = o;
+      rec[1] = dst;
+      rec[2] = b0;
+      rec[3] = nb;
+      rec[4] = vrows;
+      rec[5] = p.a[PA_BAND_DST_ROW][rb + b0];
+      rec[7] = nch;
+      atomicAdd(&p.a[PA_GROUP_NCHUNK][o * W + dst], nch);
+    }
+    int tot;
+    const int cb = chunk_carry + block_excl_scan(nch, scratch, &tot);
+    if (idx < nsegs) {
+      rec[6] = cb;
+      int32_t* out = p.a[PA_SEG_REC] + (size_t)idx * kSegRec;
+#pragma unroll
+      for (int q = 0; q < kSegRec; ++q) out[q] = rec[q];
+    }
+    chunk_carry += tot;
+  }
   if (tid == 0) {
-    p.a[PA_TOTALS][1] = carry;
+    p.a[PA_TOTALS][1] = nsegs;
+    p.a[PA_TOTALS][4] = chunk_carry;
     int bands = 0;
     for (int o = 0; o < W; ++o) bands += s_nb[o];
     p.a[PA_TOTALS][3] = bands;
@@ -492,28 +532,50 @@ __global__ void __launch_bounds__(1024) plan_order_kernel(DevPlan p) {
 }
 
 // Layout gather: X rows of every owner from its tokens' rows, zero rows elsewhere
-// (padding, block tails, and up to the next 128-row boundary). One warp per row.
+// (padding, block tails, and up to the next 128-row boundary). One warp per row,
+// over the rows that exist (their count is read on the device); each lane keeps
+// up to 8 independent 16-byte loads in flight.
 struct GatherPtrs {
   const __nv_bfloat16* x[MOE_MAX_RANKS];
   __nv_bfloat16* xb[MOE_MAX_RANKS];
 };
 
-__global__ void layout_gather_kernel(DevPlan p, GatherPtrs g) {
+__global__ void layout_gather_kernel(DevPlan p, const __grid_constant__ GatherPtrs g) {
   const Dims d = p.d;
   const int lane = threadIdx.x & 31;
+  int end[MOE_MAX_RANKS];  // cumulative rows to write, per owner
+  int total = 0;
+#pragma unroll
+  for (int o = 0; o < MOE_MAX_RANKS; ++o) {
+    if (o < d.W) total += min(d.RM, roundup(p.a[PA_RANK_ROWS][o], kTileM));
+    end[o] = total;
+  }
+  const int n16 = d.D / 8;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int n16 = d.D / 8;  // 16-byte chunks per row
-  for (long long gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; gw < (long long)d.W * d.RM;
-       gw += warps) {
-    const int o = (int)(gw / d.RM), r = (int)(gw % d.RM);
+  for (int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; gw < total; gw += warps) {
+    int o = 0;
+#pragma unroll
+    for (int q = 0; q < MOE_MAX_RANKS - 1; ++q) o += (q < d.W - 1 && gw >= end[q]) ? 1 : 0;
+    const int r = gw - (o > 0 ? end[o - 1] : 0);
     const int rows = p.a[PA_RANK_ROWS][o];
-    if (r >= min(d.RM, roundup(rows, kTileM))) continue;
     const int src = r < rows ? p.a[PA_XSRC][(size_t)o * d.RM + r] : -1;
     uint4* dst = reinterpret_cast<uint4*>(g.xb[o] + (size_t)r * d.D);
     if (src >= 0) {
       const int s = src / d.T, t = src % d.T;
       const uint4* sp = reinterpret_cast<const uint4*>(g.x[s] + (size_t)t * d.D);
-      for (int c = lane; c < n16; c += 32) dst[c] = __ldg(sp + c);
+      for (int c0 = 0; c0 < n16; c0 += 8 * 32) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + u * 32 + lane;
+          if (c < n16) v[u] = __ldg(sp + c);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + u * 32 + lane;
+          if (c < n16) dst[c] = v[u];
+        }
+      }
     } else {
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int c = lane; c < n16; c += 32) dst[c] = z;
@@ -522,6 +584,17 @@ __global__ void layout_gather_kernel(DevPlan p, GatherPtrs g) {
 }
 
 }  // namespace
+
+cudaError_t preload_plan() {
+  cudaFuncAttributes fa;
+  cudaError_t e;
+  if ((e = cudaFuncGetAttributes(&fa, plan_bitmap_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, plan_count_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, plan_rank_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, plan_scatter_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, plan_order_kernel)) != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&fa, layout_gather_kernel);
+}
 
 cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s) {
   const Dims& d = p.d;
@@ -543,7 +616,7 @@ cudaError_t launch_gather(const DevPlan& p, const __nv_bfloat16* const* x,
     g.x[r] = x[r];
     g.xb[r] = xbuf[r];
   }
-  layout_gather_kernel<<<num_sms * 8, 256, 0, s>>>(p, g);
+  layout_gather_kernel<<<num_sms * 16, 256, 0, s>>>(p, g);
   return cudaGetLastError();
 }
 

@@ -78,41 +78,52 @@ __global__ void route_kernel(DevPlan p, const float* __restrict__ logits,
   }
 }
 
-// One warp per token (s, t): out_s[t] = sum_j w_j * row_j, fp32 in slot order.
+// One thread per 16-byte chunk (8 columns) of one token's output (the grid covers
+// every chunk exactly):
+// out_s[t][c] = sum_j w_j * row_j[c], fp32 in slot order. The k row loads of a
+// thread are independent, so they are all in flight together.
 __global__ void scale_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
   const int n16 = d.D / 8;
-  for (int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < d.W * d.T; tok += warps) {
+  const long long total = (long long)d.W * d.T * n16;
+  {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int tok = (int)(i / n16), c = (int)(i % n16);
     const int s = tok / d.T, t = tok % d.T;
     const int32_t* src = a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k;
     const float* wt = a.w + (size_t)tok * d.k;
-    uint4* out = reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D);
-    for (int c = lane; c < n16; c += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < d.k; ++j) {
-        const int sj = src[j];
-        if (sj == INT_MIN) continue;  // invalid routing slot (reported by the plan)
-        const __nv_bfloat16* row =
-            sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
-        const float wj = wt[j];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int j = 0; j < d.k; ++j) {
+      const int sj = src[j];
+      if (sj == INT_MIN) continue;  // invalid routing slot (reported by the plan)
+      const __nv_bfloat16* row =
+          sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
+      const float wj = wt[j];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(h[q]);
-          acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
-          acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
+        acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
       }
-      out[c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                          pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
+    reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D)[c] =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
   }
 }
 
 }  // namespace
+
+cudaError_t preload_route_scale() {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, route_kernel);
+  if (e != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&fa, scale_kernel);
+}
 
 cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* forced,
                          int32_t* ids, float* w, cudaStream_t s) {
@@ -122,7 +133,9 @@ cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* f
 }
 
 cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s) {
-  scale_kernel<<<num_sms * 8, 256, 0, s>>>(a);
+  (void)num_sms;
+  const long long total = (long long)a.p.d.W * a.p.d.T * (a.p.d.D / 8);
+  scale_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
