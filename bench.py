@@ -257,6 +257,24 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=5):
             ser.setdefault(name, []).append(t[i])
     ser = {n: statistics.median(v) for n, v in ser.items()}
     del serial
+    # Consumer CTAs beside the producer: whole-step time for a few partitions.
+    sweep = {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for cc in [c for c in args.ccta_sweep if c >= 0]:
+        lay = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, cc)
+        for _ in range(3):
+            lay.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                        producer=sp, consumer=sc)
+        torch.cuda.synchronize()
+        ev0.record(sp)
+        for _ in range(iters * 4):
+            lay.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                        producer=sp, consumer=sc)
+        ev1.record(sp)
+        torch.cuda.synchronize()
+        sweep[str(cc)] = ev0.elapsed_time(ev1) / (iters * 4)
+        lay.close()
+        del lay
     rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
     recv_rows = layer.field(capi.MOE_PLAN_RECV_ROWS).cpu().tolist()
     rows = sum(rank_rows)
@@ -269,6 +287,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=5):
     return {
         "overlapped_ms": over,
         "serial_ms": ser,
+        "step_ms_by_consumer_ctas": sweep,
         "producer_alone_tflops": flops / (ser["producer"] * 1e-3) / 1e12,
         "producer_alone_frac_burst": flops / (ser["producer"] * 1e-3) / 1e12 / bf16,
         "producer_overlapped_tflops": flops / (over["producer"] * 1e-3) / 1e12,
@@ -407,6 +426,10 @@ def main():
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ccta-sweep", type=lambda v: [int(x) for x in v.split(",") if x],
+                    default=[0, 2, 4, 8, 16],
+                    help="consumer-CTA counts whose step time is reported (outside the timed "
+                         "region); 0 is the serial schedule")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -78,41 +78,67 @@ __global__ void route_kernel(DevPlan p, const float* __restrict__ logits,
   }
 }
 
-// One thread per 16-byte chunk (8 columns) of one token's output (the grid covers
-// every chunk exactly):
-// out_s[t][c] = sum_j w_j * row_j[c], fp32 in slot order. The k row loads of a
-// thread are independent, so they are all in flight together.
+// One thread per 16-byte chunk (8 columns) of the outputs of kScaleTok tokens
+// that are total/kScaleTok apart: out_s[t][c] = sum_j w_j * row_j[c], fp32 in slot
+// order. Each token's row addresses depend on its scale-map entry, so a thread
+// keeps the chains of its tokens independent and all their loads in flight.
+constexpr int kScaleTok = 2;
+
 __global__ void scale_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
   const int n16 = d.D / 8;
   const long long total = (long long)d.W * d.T * n16;
-  {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= total) return;
-    const int tok = (int)(i / n16), c = (int)(i % n16);
-    const int s = tok / d.T, t = tok % d.T;
-    const int32_t* src = a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k;
-    const float* wt = a.w + (size_t)tok * d.k;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int j = 0; j < d.k; ++j) {
-      const int sj = src[j];
-      if (sj == INT_MIN) continue;  // invalid routing slot (reported by the plan)
-      const __nv_bfloat16* row =
-          sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
-      const float wj = wt[j];
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+  const long long span = (total + kScaleTok - 1) / kScaleTok;
+  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i0 >= span) return;
+  float acc[kScaleTok][8];
+  int tok[kScaleTok], c[kScaleTok];
+  bool live[kScaleTok];
+#pragma unroll
+  for (int u = 0; u < kScaleTok; ++u) {
+    const long long i = i0 + u * span;
+    live[u] = i < total;
+    tok[u] = live[u] ? (int)(i / n16) : 0;
+    c[u] = live[u] ? (int)(i % n16) : 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
+  }
+  for (int j = 0; j < d.k; ++j) {
+    int sj[kScaleTok];
+    float wj[kScaleTok];
+#pragma unroll
+    for (int u = 0; u < kScaleTok; ++u) {
+      sj[u] = live[u] ? a.p.a[PA_SCALE_SRC][(size_t)tok[u] * d.k + j] : INT_MIN;
+      wj[u] = live[u] ? a.w[(size_t)tok[u] * d.k + j] : 0.f;
+    }
+    uint4 v[kScaleTok];
+#pragma unroll
+    for (int u = 0; u < kScaleTok; ++u) {
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (sj[u] == INT_MIN) continue;  // invalid routing slot (reported by the plan)
+      const int s = tok[u] / d.T;
+      const __nv_bfloat16* row = sj[u] >= 0 ? a.recv[s] + (size_t)sj[u] * d.D
+                                            : a.y[s] + (size_t)(-sj[u] - 1) * d.D;
+      v[u] = __ldg(reinterpret_cast<const uint4*>(row) + c[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kScaleTok; ++u) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float2 f = __bfloat1622float2(h[q]);
-        acc[2 * q] = fmaf(wj, f.x, acc[2 * q]);
-        acc[2 * q + 1] = fmaf(wj, f.y, acc[2 * q + 1]);
+        acc[u][2 * q] = fmaf(wj[u], f.x, acc[u][2 * q]);
+        acc[u][2 * q + 1] = fmaf(wj[u], f.y, acc[u][2 * q + 1]);
       }
     }
-    reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D)[c] =
-        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+#pragma unroll
+  for (int u = 0; u < kScaleTok; ++u) {
+    if (!live[u]) continue;
+    const int s = tok[u] / d.T, t = tok[u] % d.T;
+    reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D)[c[u]] =
+        make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
+                   pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
   }
 }
 
@@ -135,7 +161,8 @@ cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* f
 cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s) {
   (void)num_sms;
   const long long total = (long long)a.p.d.W * a.p.d.T * (a.p.d.D / 8);
-  scale_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a);
+  const long long span = (total + kScaleTok - 1) / kScaleTok;
+  scale_kernel<<<(unsigned)((span + 255) / 256), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
