@@ -81,6 +81,7 @@ def load():
         "moe_field": (ip, [P(moe_cfg), ip, P(sz), P(sz)]),
         "moe_set_timing": (ip, [vp, ip]),
         "moe_timings": (ip, [vp, P(ctypes.c_float), ip]),
+        "moe_plan_build_noalloc": (ip, [P(moe_cfg), vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -174,3 +175,8 @@ def moe_timings(plan, n: int = 6):
     buf = (ctypes.c_float * n)()
     check(lib().moe_timings(plan, buf, n), "moe_timings")
     return list(buf)
+
+
+def moe_plan_build_noalloc(cfg: moe_cfg, topk_ids, plan_out, plan_out_bytes, stream):
+    check(lib().moe_plan_build_noalloc(ctypes.byref(cfg), topk_ids, plan_out, plan_out_bytes,
+                                       stream), "moe_plan_build_noalloc")
