@@ -67,6 +67,7 @@ int dims_from_cfg(const moe_cfg* c, Dims* d) {
                        (long long)c->L * c->W * (c->tb_M - 1);
   const long long RM = (rm + c->tb_M - 1) / c->tb_M * c->tb_M;
   if (RM >= (1LL << 24)) return MOE_ERR_UNSUPPORTED;
+  if ((long long)c->W * c->T * (c->d_model / 8) >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   x.RM = (int)RM;
   x.NBM = x.RM / x.tb;
   x.parts = x.tb >= kTileM ? x.tb / kTileM : 1;

@@ -14,11 +14,12 @@
 // the consumer CTAs, so every CTA follows production and the last segment is
 // copied by all of them. A CTA is one warp: the lanes poll the flags of a chunk's
 // bands together, and lane 0 moves the chunk with TMA bulk copies through a
-// three-slot shared-memory ring (global -> shared completes on an mbarrier,
+// six-slot shared-memory ring (global -> shared completes on an mbarrier,
 // shared -> global as a bulk group). A group is (sender o, destination s). When a
-// CTA has stored the last of its chunks of a group it waits for those stores,
-// issues one fence and one release increment of the group's chunk count; the
-// increment that completes the group stores the group signal.
+// CTA has stored the last of its chunks of a group, the group joins a release
+// batch: at the CTA's next wait (or its end) it waits for its stores, issues one
+// fence for the whole batch and one release increment of each group's chunk
+// count; the increment that completes a group stores the group signal.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -78,9 +79,11 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   __syncwarp();
 
   // Copy pipeline, driven by lane 0. Chunk i (in this CTA's order) uses slot i % S
-  // and completes phase (i / S) & 1 of that slot's barrier. At most two loads are
-  // outstanding; a slot is refilled only after the store that last used it has
-  // finished reading it.
+  // and completes phase (i / S) & 1 of that slot's barrier. A chunk is stored as
+  // soon as its load has landed; at most kLoadsInFlight loads are outstanding, so
+  // when a slot is refilled at least S - kLoadsInFlight newer stores follow the
+  // store that last used it, and waiting until only that many may still be reading
+  // frees the slot without waiting for recent stores.
   struct Pend {
     uint8_t* dst;
     uint32_t bytes;
@@ -88,10 +91,11 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   };
   Pend pend[kChunkSlots] = {};
   int n = 0, stored = 0;
+  unsigned long long finished = 0;  // groups whose chunks (of this CTA) are all stored
   bool ok = true;
   const long long itimeout = a.p.timeout_ns + 4000000000LL;
 
-  auto store_next = [&]() {  // lane 0: store chunk `stored` once its load has landed
+  auto store_one = [&]() {  // lane 0: store chunk `stored` (bounded wait for its load)
     const int slot = stored % kChunkSlots;
     volatile int never = 0;
     if (!mbar_wait_bounded(&sm.full[slot], (stored / kChunkSlots) & 1, &never, itimeout, status,
@@ -101,11 +105,22 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     bulk_commit();
     ++stored;
     const int g = pend[slot].group;
-    if (--sm.owned[g] == 0) {
-      // This CTA's last chunk of group g: one fence for all of them, then the count.
-      bulk_wait_all();
-      fence_proxy_async_global();
-      fence_acq_rel_gpu();
+    if (--sm.owned[g] == 0) finished |= 1ull << g;
+  };
+  auto store_landed = [&]() {  // lane 0: store every leading chunk whose load has landed
+    while (stored < n && mbar_try_wait(&sm.full[stored % kChunkSlots], (stored / kChunkSlots) & 1))
+      store_one();
+  };
+  // One fence for every group this CTA has finished since the last release, then
+  // one count increment per group; the increment that completes a group signals it.
+  auto release_finished = [&]() {
+    if (finished == 0) return;
+    bulk_wait_all();
+    fence_proxy_async_global();
+    fence_acq_rel_gpu();
+    while (finished) {
+      const int g = __ffsll((long long)finished) - 1;
+      finished &= finished - 1;
       const uint32_t mine = (uint32_t)sm.total[g];
       const uint32_t done = atomicAdd(group_done + g, mine) + mine;
       if (done == (uint32_t)gchunks[g]) st_release_u32(group_sig + g, 1u);
@@ -130,18 +145,31 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     return ready;
   };
 
-  int base = 0;
+  // Records are read a batch of 32 ahead: each lane keeps the record it will
+  // publish for the next batch in registers, so that load's latency overlaps the
+  // copies of the current batch.
+  int nextrec[kSegRec];
+  auto fetch = [&](int b) {
+    if (b + lane < nseg) {
+      const int32_t* r = recs + (size_t)(b + lane) * kSegRec;
+#pragma unroll
+      for (int q = 0; q < kSegRec; ++q) nextrec[q] = r[q];
+    }
+  };
+  fetch(0);
+  int base = 0, fetched = 0;
   while (base < nseg && ok) {
-    // Load up to 32 records and list this CTA's chunks of as many of them as fit.
+    // Publish up to 32 records (the prefetched ones when they start at `base`).
     const int nb = min(32, nseg - base);
     __syncwarp();
-    int cnt = 0;
+    if (fetched != base) fetch(base);
     if (lane < nb) {
-      const int32_t* r = recs + (size_t)(base + lane) * kSegRec;
 #pragma unroll
-      for (int q = 0; q < kSegRec; ++q) sm.rec[lane][q] = r[q];
-      cnt = owned_count(r[6], r[7], c, G);
+      for (int q = 0; q < kSegRec; ++q) sm.rec[lane][q] = nextrec[q];
     }
+    __syncwarp();
+    int cnt = 0;
+    if (lane < nb) cnt = owned_count(sm.rec[lane][6], sm.rec[lane][7], c, G);
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -153,6 +181,8 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     const unsigned fit = __ballot_sync(0xffffffffu, lane < nb && incl <= kListCap);
     const int take = max(1, __popc(fit));
     const int nlist = __shfl_sync(0xffffffffu, incl, take - 1);
+    fetch(base + take);
+    fetched = base + take;
     if (lane < take && cnt > 0) {
       const int cb = sm.rec[lane][6];
       int k = ((c - cb) % G + G) % G;
@@ -176,8 +206,10 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
         chunk_of(sm.list[s0 + j], q, r0, r1);
         if (!(ready >> j & 1u)) {
           // Not produced yet: store everything loaded, then wait (bounded, all lanes).
-          if (lane == 0)
-            while (stored < n) store_next();
+          if (lane == 0) {
+            while (stored < n) store_one();
+            release_finished();
+          }
           const unsigned long long t0 = globaltimer();
           bool done = false, stop = false;
           while (!done && !stop) {
@@ -212,8 +244,9 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
         }
         if (lane == 0) {
           fence_proxy_async_global();  // the flags were acquired; the bulk load reads Y
-          if (n - stored == kChunkSlots) store_next();
-          if (n >= kChunkSlots) bulk_wait_read<0>();  // the slot's last store has read it
+          store_landed();
+          while (n - stored >= kLoadsInFlight) store_one();
+          if (n >= kChunkSlots) bulk_wait_read<kChunkSlots - kLoadsInFlight>();
           const int o = sm.rec[q][0], dst = sm.rec[q][1], b0 = sm.rec[q][2];
           const int slot = n % kChunkSlots;
           const uint32_t bytes = (uint32_t)((size_t)(r1 - r0) * row_bytes);
@@ -235,7 +268,8 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   if (lane == 0) {
     // Drain: store what was loaded (even after an error, so no copy outlives the
     // CTA's shared memory), then wait for every store.
-    while (stored < n) store_next();
+    while (stored < n) store_one();
+    release_finished();
     bulk_wait_all();
   }
 }

@@ -87,19 +87,19 @@ constexpr int kScaleTok = 2;
 __global__ void scale_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
   const int n16 = d.D / 8;
-  const long long total = (long long)d.W * d.T * n16;
-  const long long span = (total + kScaleTok - 1) / kScaleTok;
-  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int total = d.W * d.T * n16;  // < 2^31 (checked when the plan is created)
+  const int span = (total + kScaleTok - 1) / kScaleTok;
+  const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
   if (i0 >= span) return;
   float acc[kScaleTok][8];
   int tok[kScaleTok], c[kScaleTok];
   bool live[kScaleTok];
 #pragma unroll
   for (int u = 0; u < kScaleTok; ++u) {
-    const long long i = i0 + u * span;
+    const int i = i0 + u * span;
     live[u] = i < total;
-    tok[u] = live[u] ? (int)(i / n16) : 0;
-    c[u] = live[u] ? (int)(i % n16) : 0;
+    tok[u] = live[u] ? i / n16 : 0;
+    c[u] = live[u] ? i - tok[u] * n16 : 0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
   }
