@@ -419,7 +419,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--consumer-ctas", type=int, default=8,
+    ap.add_argument("--consumer-ctas", type=int, default=4,
                     help="consumer CTAs beside the producer; 0 runs the two kernels serially "
                          "(needed under a profiler, which serialises kernel launches)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,

@@ -99,3 +99,20 @@ def test_host_errors_without_a_device(lib):
     assert lib_.moe_plan_build(None, None, None, None) == capi.MOE_ERR_ARG
     assert lib_.moe_scale(None, None, None, None, None) == capi.MOE_ERR_ARG
     assert lib_.moe_set_timing(None, 1) == capi.MOE_ERR_ARG
+
+
+@pytest.mark.parametrize("shape", [
+    dict(W=3, L=3, topk=2, T=77, d_model=256, d_ff=384, tb_M=64, mgb=3),
+    dict(W=4, L=2, topk=3, T=130, d_model=128, d_ff=256, tb_M=128),
+    dict(W=8, L=32, topk=8, T=256, d_model=7168, d_ff=2048, tb_M=64),
+    dict(W=1, L=3, topk=2, T=50, d_model=128, d_ff=256, tb_M=128),
+])
+def test_plan_arrays_are_aligned(lib, shape):
+    """Kernels read plan arrays with 16-byte vector loads: every array outside the
+    packed per-combine region (ready flags, group signals) starts on 256 bytes."""
+    c = _cfg(**shape)
+    for name, v in capi.ENUMS.items():
+        if name.startswith("MOE_PLAN_") and name not in ("MOE_PLAN_NFIELDS", "MOE_PLAN_FLAGS",
+                                                         "MOE_PLAN_GROUP_SIG"):
+            off, _ = capi.moe_field(c, v)
+            assert off % 256 == 0, (name, off)

@@ -114,9 +114,10 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;
     if (cnt) cnt[i] = n[i];
-    // The per-combine zeroed arrays are packed back to back (one memset).
+    // The per-combine zeroed arrays are packed back to back (one memset); every
+    // array after them starts on a kAlign boundary again.
     const bool packed = i >= PA_QUEUE && i < PA_GROUP_SIG;
-    pos += packed ? n[i] * 4 : align_up(n[i] * 4, kAlign);
+    pos = packed ? pos + n[i] * 4 : align_up(pos + n[i] * 4, kAlign);
   }
   return align_up(pos, kAlign);
 }

@@ -28,13 +28,15 @@ namespace {
 constexpr int kMaxGroups = MOE_MAX_RANKS * MOE_MAX_RANKS;
 
 constexpr int kListCap = kMaxSegChunks;  // owned chunks listed per batch of records
+constexpr int kRecPerLane = 8;
+constexpr int kRecBatch = 32 * kRecPerLane;  // segment records per batch
 
 struct ConsumerSmem {
   uint64_t full[kChunkSlots];
-  int owned[kMaxGroups];  // this CTA's chunks of each group not yet stored
-  int total[kMaxGroups];  // this CTA's chunks of each group
-  int rec[32][kSegRec];   // a batch of segment records
-  int list[kListCap];     // owned chunks of the batch: (record << 24) | chunk index
+  int owned[kMaxGroups];        // this CTA's chunks of each group not yet stored
+  int total[kMaxGroups];        // this CTA's chunks of each group
+  int rec[kRecBatch][kSegRec];  // a batch of segment records
+  int list[kListCap];           // owned chunks of the batch: (record << 20) | chunk index
 };
 
 static_assert(sizeof(ConsumerSmem) <= kConsumerSmemTail, "consumer shared memory layout");
@@ -68,11 +70,27 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
-  // Pre-pass: how many chunks of each group this CTA copies.
-  for (int idx = lane; idx < nseg; idx += 32) {
-    const int32_t* r = recs + (size_t)idx * kSegRec;
-    const int n = owned_count(r[6], r[7], c, G);
-    if (n) atomicAdd(&sm.owned[r[0] * d.W + r[1]], n);
+  // Pre-pass: how many chunks of each group this CTA copies (8 records per lane
+  // per round, their loads independent).
+  for (int base = 0; base < nseg; base += 32 * 8) {
+    int4 lo[8], hi[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = base + u * 32 + lane;
+      if (idx < nseg) {
+        const int4* r = reinterpret_cast<const int4*>(recs + (size_t)idx * kSegRec);
+        lo[u] = r[0];
+        hi[u] = r[1];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = base + u * 32 + lane;
+      if (idx < nseg) {
+        const int n = owned_count(hi[u].z, hi[u].w, c, G);
+        if (n) atomicAdd(&sm.owned[lo[u].x * d.W + lo[u].y], n);
+      }
+    }
   }
   __syncwarp();
   for (int g = lane; g < kMaxGroups; g += 32) sm.total[g] = sm.owned[g];
@@ -129,11 +147,12 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
 
   // Rows and flags of listed chunk `e` (a packed list entry).
   auto chunk_of = [&](int e, int& q, int& r0, int& r1) {
-    q = e >> 24;
-    const int k = e & 0xFFFFFF;
+    q = e >> 20;
+    const int k = e & 0xFFFFF;
     r0 = k * d.rpc;
     r1 = min(sm.rec[q][4], r0 + d.rpc);
   };
+  // Acquire reads of the ready flags of one chunk (a subset of them per lane).
   auto flags_ready = [&](int q, int r0, int r1, int lane_lo, int lane_step) {
     const int b0 = sm.rec[q][2];
     const size_t rb = (size_t)sm.rec[q][0] * d.NBM;
@@ -145,67 +164,87 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     return ready;
   };
 
-  // Records are read a batch of 32 ahead: each lane keeps the record it will
-  // publish for the next batch in registers, so that load's latency overlaps the
-  // copies of the current batch.
-  int nextrec[kSegRec];
-  auto fetch = [&](int b) {
-    if (b + lane < nseg) {
-      const int32_t* r = recs + (size_t)(b + lane) * kSegRec;
-#pragma unroll
-      for (int q = 0; q < kSegRec; ++q) nextrec[q] = r[q];
-    }
-  };
-  fetch(0);
-  int base = 0, fetched = 0;
+  // Records are taken in batches of up to kRecBatch (8 per lane, loads
+  // independent). Each batch lists this CTA's chunks of as many of its records as
+  // fit in kListCap entries, in order; the flags of 64 listed chunks are checked
+  // per round trip (2 per lane).
+  int base = 0;
   while (base < nseg && ok) {
-    // Publish up to 32 records (the prefetched ones when they start at `base`).
-    const int nb = min(32, nseg - base);
+    int cnt[kRecPerLane];
+    int lsum = 0;
     __syncwarp();
-    if (fetched != base) fetch(base);
-    if (lane < nb) {
 #pragma unroll
-      for (int q = 0; q < kSegRec; ++q) sm.rec[lane][q] = nextrec[q];
+    for (int u = 0; u < kRecPerLane; ++u) {
+      const int ri = lane * kRecPerLane + u;  // record of the batch, in order
+      const int idx = base + ri;
+      cnt[u] = 0;
+      if (idx < nseg) {
+        const int4* r = reinterpret_cast<const int4*>(recs + (size_t)idx * kSegRec);
+        const int4 lo = r[0], hi = r[1];
+        sm.rec[ri][0] = lo.x; sm.rec[ri][1] = lo.y; sm.rec[ri][2] = lo.z; sm.rec[ri][3] = lo.w;
+        sm.rec[ri][4] = hi.x; sm.rec[ri][5] = hi.y; sm.rec[ri][6] = hi.z; sm.rec[ri][7] = hi.w;
+        cnt[u] = owned_count(hi.z, hi.w, c, G);
+      }
+      lsum += cnt[u];
     }
-    __syncwarp();
-    int cnt = 0;
-    if (lane < nb) cnt = owned_count(sm.rec[lane][6], sm.rec[lane][7], c, G);
-    int incl = cnt;
+    int incl = lsum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    // Records taken: every lane whose inclusive count fits (the first always fits,
+    // Records that fit: a prefix of the batch (the first record always fits,
     // because a segment has at most kListCap chunks).
-    const unsigned fit = __ballot_sync(0xffffffffu, lane < nb && incl <= kListCap);
-    const int take = max(1, __popc(fit));
-    const int nlist = __shfl_sync(0xffffffffu, incl, take - 1);
-    fetch(base + take);
-    fetched = base + take;
-    if (lane < take && cnt > 0) {
-      const int cb = sm.rec[lane][6];
-      int k = ((c - cb) % G + G) % G;
-      for (int j = 0, pos = incl - cnt; j < cnt; ++j, ++pos, k += G) sm.list[pos] = (lane << 24) | k;
+    int pos = incl - lsum, fit = 0;
+#pragma unroll
+    for (int u = 0; u < kRecPerLane; ++u) {
+      const int idx = base + lane * kRecPerLane + u;
+      if (idx < nseg && pos + cnt[u] <= kListCap) {
+        const int ri = lane * kRecPerLane + u;
+        int k = ((c - sm.rec[ri][6]) % G + G) % G;
+        for (int j = 0; j < cnt[u]; ++j, k += G) sm.list[pos + j] = (ri << 20) | k;
+        pos += cnt[u];
+        ++fit;
+      } else {
+        pos = kListCap + 1;  // later records of the batch wait for the next batch
+      }
+    }
+    int take = fit;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) take += __shfl_xor_sync(0xffffffffu, take, o);
+    take = max(1, take);
+    int nlist = 0;
+    {  // entries written by the fitting records
+      const int last = take - 1;  // last fitting record of the batch
+      const int ll = last / kRecPerLane;
+      int e = incl - lsum;
+      for (int u = 0; u <= last - ll * kRecPerLane; ++u) e += cnt[u];
+      nlist = __shfl_sync(0xffffffffu, e, ll);
     }
     __syncwarp();
 
-    // Walk the listed chunks 32 at a time: every lane checks one chunk's flags, so
-    // the flag latency is paid once per 32 chunks while copies are in flight.
-    for (int s0 = 0; s0 < nlist && ok; s0 += 32) {
-      const int m = min(32, nlist - s0);
-      bool mine = true;
+    for (int s0 = 0; s0 < nlist && ok; s0 += 64) {
+      const int m = min(64, nlist - s0);
+      bool r0ok = true, r1ok = true;
       if (lane < m) {
-        int q, r0, r1;
-        chunk_of(sm.list[s0 + lane], q, r0, r1);
-        mine = flags_ready(q, r0, r1, 0, 1);
+        int q, a0, a1;
+        chunk_of(sm.list[s0 + lane], q, a0, a1);
+        r0ok = flags_ready(q, a0, a1, 0, 1);
       }
-      unsigned ready = __ballot_sync(0xffffffffu, mine);
+      if (lane + 32 < m) {
+        int q, a0, a1;
+        chunk_of(sm.list[s0 + 32 + lane], q, a0, a1);
+        r1ok = flags_ready(q, a0, a1, 0, 1);
+      }
+      unsigned long long ready = (unsigned long long)__ballot_sync(0xffffffffu, r0ok) |
+                                 ((unsigned long long)__ballot_sync(0xffffffffu, r1ok) << 32);
+      __syncwarp();  // orders lane 0's copies after every lane's acquire
       for (int j = 0; j < m && ok; ++j) {
         int q, r0, r1;
         chunk_of(sm.list[s0 + j], q, r0, r1);
-        if (!(ready >> j & 1u)) {
-          // Not produced yet: store everything loaded, then wait (bounded, all lanes).
+        if (!(ready >> j & 1ull)) {
+          // Not produced yet: store everything loaded, release finished groups,
+          // then wait (bounded, all lanes).
           if (lane == 0) {
             while (stored < n) store_one();
             release_finished();
@@ -234,13 +273,21 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
             break;
           }
           // Chunks after this one may have become ready meanwhile.
-          bool again = true;
+          bool a0ok = true, a1ok = true;
           if (lane > j && lane < m) {
-            int q2, a0, a1;
-            chunk_of(sm.list[s0 + lane], q2, a0, a1);
-            again = flags_ready(q2, a0, a1, 0, 1);
+            int q2, b0, b1;
+            chunk_of(sm.list[s0 + lane], q2, b0, b1);
+            a0ok = flags_ready(q2, b0, b1, 0, 1);
           }
-          ready = __ballot_sync(0xffffffffu, again) | ((1u << j) << 1) - 1u;
+          if (lane + 32 > j && lane + 32 < m) {
+            int q2, b0, b1;
+            chunk_of(sm.list[s0 + 32 + lane], q2, b0, b1);
+            a1ok = flags_ready(q2, b0, b1, 0, 1);
+          }
+          ready = (unsigned long long)__ballot_sync(0xffffffffu, a0ok) |
+                  ((unsigned long long)__ballot_sync(0xffffffffu, a1ok) << 32);
+          ready |= j == 63 ? ~0ull : ((1ull << (j + 1)) - 1ull);
+          __syncwarp();
         }
         if (lane == 0) {
           fence_proxy_async_global();  // the flags were acquired; the bulk load reads Y

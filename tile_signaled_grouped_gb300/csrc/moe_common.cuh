@@ -20,13 +20,13 @@ constexpr int kBlockK = 64;      // K elements per pipeline stage (128 B of bf16
 constexpr int kN1 = 128;         // GEMM1 hidden columns per tile (gate and up each)
 constexpr int kStages = 4;       // shared-memory pipeline depth
 constexpr int kTaskRing = 4;     // task descriptors in flight inside one CTA
-constexpr int kTileGroup = 8;    // tiles per scheduling unit (weight reuse in L2)
+constexpr int kTileGroup = 32;   // tiles per scheduling unit (weight reuse in L2)
 constexpr int kProducerThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kConsumerThreads = 32;         // one warp: lane 0 drives the bulk copies
 constexpr int kChunkBytes = 20 * 1024;       // consumer copy chunk (one shared-memory slot)
 constexpr int kChunkSlots = 6;               // 120 KB: keeps one consumer CTA alone on its SM
 constexpr int kLoadsInFlight = 4;            // consumer bulk loads outstanding at most
-constexpr size_t kConsumerSmemTail = 4096;  // barriers, counters and records after the slots
+constexpr size_t kConsumerSmemTail = 12 * 1024;  // barriers, counters and records after the slots
 constexpr size_t kConsumerSmem = (size_t)kChunkSlots * kChunkBytes + kConsumerSmemTail;
 constexpr int kSegRec = 8;                   // ints per consumer segment record
 constexpr int kMaxSegChunks = 256;           // copy chunks one segment may have
