@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   };
   // One fence for every group this CTA has finished since the last release, then
   // one count increment per group; the increment that completes a group signals it.
-  auto release_finished = [&]() {
+  auto release_finished = [&]() {  // lane 0
     if (finished == 0) return;
     bulk_wait_all();
     fence_proxy_async_global();
@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
       unsigned long long ready = (unsigned long long)__ballot_sync(0xffffffffu, r0ok) |
                                  ((unsigned long long)__ballot_sync(0xffffffffu, r1ok) << 32);
       __syncwarp();  // orders lane 0's copies after every lane's acquire
+      // The flags were acquired (generic proxy); the bulk loads read Y (async proxy).
+      if (lane == 0) fence_proxy_async_global();
       for (int j = 0; j < m && ok; ++j) {
         int q, r0, r1;
         chunk_of(sm.list[s0 + j], q, r0, r1);
@@ -288,9 +290,9 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
                   ((unsigned long long)__ballot_sync(0xffffffffu, a1ok) << 32);
           ready |= j == 63 ? ~0ull : ((1ull << (j + 1)) - 1ull);
           __syncwarp();
+          if (lane == 0) fence_proxy_async_global();
         }
         if (lane == 0) {
-          fence_proxy_async_global();  // the flags were acquired; the bulk load reads Y
           store_landed();
           while (n - stored >= kLoadsInFlight) store_one();
           if (n >= kChunkSlots) bulk_wait_read<kChunkSlots - kLoadsInFlight>();
@@ -312,9 +314,9 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     }
     base += take;
   }
+  // Drain: store what was loaded (even after an error, so no copy outlives the
+  // CTA's shared memory), release the finished groups, wait for every store.
   if (lane == 0) {
-    // Drain: store what was loaded (even after an error, so no copy outlives the
-    // CTA's shared memory), then wait for every store.
     while (stored < n) store_one();
     release_finished();
     bulk_wait_all();

@@ -14,8 +14,10 @@
 //     adds one release increment to the ready flag of every row band it covers.
 // Tasks come from one atomic ticket counter. Tickets decode to scheduling
 // units of up to kTileGroup tiles: a unit's GEMM1 tasks are emitted `lag`
-// units ahead of its GEMM2 tasks, hidden-column-major inside the unit so that
-// consecutive tickets reuse the same weight tile from L2. A GEMM2 task waits
+// units ahead of its GEMM2 tasks. GEMM1 tasks are hidden-column-major inside the
+// unit, so consecutive tickets reuse one gate/up weight tile from L2; GEMM2 tasks
+// are tile-major, so a tile's hidden activations are read once while the
+// expert's W_down tiles stay in L2. A GEMM2 task waits
 // (bounded) until its block's GEMM1 tiles are all counted; the waits only ever
 // point at lower tickets, which are held by running CTAs, so the kernel cannot
 // deadlock.
@@ -102,9 +104,10 @@ __device__ Task decode_ticket(const Smem& sm, const ProducerArgs& a, long long t
     r -= (long long)d.nt1 * sz1;
     const int u2 = u - a.lag;
     const int sz2 = unit_at(sm, gub, u2 + 1) - unit_at(sm, gub, u2);
+    (void)sz2;
     tk.kind = kG2;
-    tk.m = unit_at(sm, gub, u2) + (int)(r % sz2);
-    tk.nt = (int)(r / sz2);
+    tk.m = unit_at(sm, gub, u2) + (int)(r / d.nt2);  // tile-major: a tile's hidden rows
+    tk.nt = (int)(r % d.nt2);                         // stay in L2 for its nt2 tasks
   }
   const int tr = a.p.a[PA_TILE_ROW][tk.m];
   tk.o = tr >> 24;

@@ -4,6 +4,8 @@
 // router forms a probability distribution over the E experts per token and
 // keeps the top k; the owner rank combines the k expert outputs of a token
 // with the gate weights.
+#include <algorithm>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -78,67 +80,56 @@ __global__ void route_kernel(DevPlan p, const float* __restrict__ logits,
   }
 }
 
-// One thread per 16-byte chunk (8 columns) of the outputs of kScaleTok tokens
-// that are total/kScaleTok apart: out_s[t][c] = sum_j w_j * row_j[c], fp32 in slot
-// order. Each token's row addresses depend on its scale-map entry, so a thread
-// keeps the chains of its tokens independent and all their loads in flight.
-constexpr int kScaleTok = 2;
-
-__global__ void scale_kernel(const __grid_constant__ ScaleArgs a) {
+// One warp per token (s, t): out_s[t] = sum_j w_j * row_j, fp32 in slot order.
+// The lanes fetch the token's scale-map entries and weights once (one round
+// trip), then each lane covers two 16-byte chunks of every row per pass, so a
+// warp keeps 2k independent 16-byte loads per lane in flight.
+__global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
+  const int lane = threadIdx.x & 31;
   const int n16 = d.D / 8;
-  const int total = d.W * d.T * n16;  // < 2^31 (checked when the plan is created)
-  const int span = (total + kScaleTok - 1) / kScaleTok;
-  const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i0 >= span) return;
-  float acc[kScaleTok][8];
-  int tok[kScaleTok], c[kScaleTok];
-  bool live[kScaleTok];
-#pragma unroll
-  for (int u = 0; u < kScaleTok; ++u) {
-    const int i = i0 + u * span;
-    live[u] = i < total;
-    tok[u] = live[u] ? i / n16 : 0;
-    c[u] = live[u] ? i - tok[u] * n16 : 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
-  }
-  for (int j = 0; j < d.k; ++j) {
-    int sj[kScaleTok];
-    float wj[kScaleTok];
-#pragma unroll
-    for (int u = 0; u < kScaleTok; ++u) {
-      sj[u] = live[u] ? a.p.a[PA_SCALE_SRC][(size_t)tok[u] * d.k + j] : INT_MIN;
-      wj[u] = live[u] ? a.w[(size_t)tok[u] * d.k + j] : 0.f;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < d.W * d.T; tok += warps) {
+    const int s = tok / d.T, t = tok % d.T;
+    int src_l = INT_MIN;
+    float w_l = 0.f;
+    if (lane < d.k) {
+      src_l = a.p.a[PA_SCALE_SRC][(size_t)tok * d.k + lane];
+      w_l = a.w[(size_t)tok * d.k + lane];
     }
-    uint4 v[kScaleTok];
+    uint4* out = reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D);
+    for (int c0 = 0; c0 < n16; c0 += 64) {
+      const int ca = c0 + lane, cb = c0 + 32 + lane;
+      float acc0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float acc1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int j = 0; j < d.k; ++j) {
+        const int sj = __shfl_sync(0xffffffffu, src_l, j);
+        const float wj = __shfl_sync(0xffffffffu, w_l, j);
+        if (sj == INT_MIN) continue;  // invalid routing slot (reported by the plan)
+        const uint4* row = reinterpret_cast<const uint4*>(
+            sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D);
+        const uint4 va = ca < n16 ? __ldg(row + ca) : make_uint4(0, 0, 0, 0);
+        const uint4 vb = cb < n16 ? __ldg(row + cb) : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&va);
+        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&vb);
 #pragma unroll
-    for (int u = 0; u < kScaleTok; ++u) {
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (sj[u] == INT_MIN) continue;  // invalid routing slot (reported by the plan)
-      const int s = tok[u] / d.T;
-      const __nv_bfloat16* row = sj[u] >= 0 ? a.recv[s] + (size_t)sj[u] * d.D
-                                            : a.y[s] + (size_t)(-sj[u] - 1) * d.D;
-      v[u] = __ldg(reinterpret_cast<const uint4*>(row) + c[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < kScaleTok; ++u) {
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(h[q]);
-        acc[u][2 * q] = fmaf(wj[u], f.x, acc[u][2 * q]);
-        acc[u][2 * q + 1] = fmaf(wj[u], f.y, acc[u][2 * q + 1]);
+        for (int q = 0; q < 4; ++q) {
+          const float2 fa = __bfloat1622float2(ha[q]);
+          const float2 fb = __bfloat1622float2(hb[q]);
+          acc0[2 * q] = fmaf(wj, fa.x, acc0[2 * q]);
+          acc0[2 * q + 1] = fmaf(wj, fa.y, acc0[2 * q + 1]);
+          acc1[2 * q] = fmaf(wj, fb.x, acc1[2 * q]);
+          acc1[2 * q + 1] = fmaf(wj, fb.y, acc1[2 * q + 1]);
+        }
       }
+      if (ca < n16)
+        out[ca] = make_uint4(pack_bf16x2(acc0[0], acc0[1]), pack_bf16x2(acc0[2], acc0[3]),
+                             pack_bf16x2(acc0[4], acc0[5]), pack_bf16x2(acc0[6], acc0[7]));
+      if (cb < n16)
+        out[cb] = make_uint4(pack_bf16x2(acc1[0], acc1[1]), pack_bf16x2(acc1[2], acc1[3]),
+                             pack_bf16x2(acc1[4], acc1[5]), pack_bf16x2(acc1[6], acc1[7]));
     }
-  }
-#pragma unroll
-  for (int u = 0; u < kScaleTok; ++u) {
-    if (!live[u]) continue;
-    const int s = tok[u] / d.T, t = tok[u] % d.T;
-    reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D)[c[u]] =
-        make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
-                   pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
   }
 }
 
@@ -159,10 +150,10 @@ cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* f
 }
 
 cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s) {
-  (void)num_sms;
-  const long long total = (long long)a.p.d.W * a.p.d.T * (a.p.d.D / 8);
-  const long long span = (total + kScaleTok - 1) / kScaleTok;
-  scale_kernel<<<(unsigned)((span + 255) / 256), 256, 0, s>>>(a);
+  // Eight warps per block, up to 16 blocks per SM: one token per warp at a time.
+  const int tokens = a.p.d.W * a.p.d.T;
+  const int blocks = std::min((tokens + 7) / 8, num_sms * 16);
+  scale_kernel<<<blocks, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
