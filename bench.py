@@ -92,6 +92,29 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def producer_traffic(wl_name: str, tokens_override: int):
+    """DRAM bytes (read + write) per producer launch, from the committed ncu summary of the
+    A100-like full-size run, while the producer's sources still hash to the fingerprint
+    recorded there; None otherwise (changed kernel, other workload)."""
+    import hashlib
+    import re
+
+    if wl_name != WORKLOAD or tokens_override:
+        return None
+    try:
+        text = open(os.path.join(ROOT, "profiles", "ffn_producer_a100_like.md")).read()
+        h = hashlib.sha256()
+        for f in ("ffn.cu", "moe_common.cuh"):
+            h.update(open(os.path.join(ROOT, "tile_signaled_grouped_gb300", "csrc", f), "rb").read())
+    except OSError:
+        return None
+    m1 = re.search(r"traffic_bytes_per_launch: (\d+)", text)
+    m2 = re.search(r"source_fingerprint: (\w+)", text)
+    if not (m1 and m2) or h.hexdigest()[:16] != m2.group(1):
+        return None
+    return int(m1.group(1))
+
+
 def max_over_ranks(v: float, device="cpu") -> float:
     """Largest value over the ranks of the default process group (v itself alone)."""
     import torch
@@ -206,7 +229,8 @@ def gpu_arm(args, rank, world, local_rank):
                    "l2": "inputs larger than L2: 768 MB of expert weights read every step"},
         "roofline": {"kernel": "ffn_producer (GEMM1+SiLU+GEMM2, executed rows)",
                      "bound": "tensor", "achieved": achieved, "peak": bf16_sus,
-                     "unit": "TFLOP/s", "frac": achieved / bf16_sus, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / bf16_sus,
+                     "traffic": producer_traffic(wl.name, args.tokens_per_rank),
                      "peak_source": f"{src} bf16 sustained (kernel timed inside a loop of steps)",
                      "flops_per_launch": flops_exec, "launch_ms": prod_avg},
         "e2e": e2e,
