@@ -92,19 +92,21 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def producer_traffic(wl_name: str, tokens_override: int):
+def producer_traffic(wl_name: str, tokens_override: int, pairs: int):
     """DRAM bytes (read + write) per producer launch, from the committed ncu summary of the
-    A100-like full-size run, while the producer's sources still hash to the fingerprint
-    recorded there; None otherwise (changed kernel, other workload)."""
+    A100-like full-size run of the producer in use, while its sources still hash to the
+    fingerprint recorded there; None otherwise (changed kernel, other workload)."""
     import hashlib
     import re
 
     if wl_name != WORKLOAD or tokens_override:
         return None
+    summary, src = (("ffn_pair_a100_like.md", "ffn_pair.cu") if pairs
+                    else ("ffn_producer_a100_like.md", "ffn.cu"))
     try:
-        text = open(os.path.join(ROOT, "profiles", "ffn_producer_a100_like.md")).read()
+        text = open(os.path.join(ROOT, "profiles", summary)).read()
         h = hashlib.sha256()
-        for f in ("ffn.cu", "moe_common.cuh"):
+        for f in (src, "moe_common.cuh"):
             h.update(open(os.path.join(ROOT, "tile_signaled_grouped_gb300", "csrc", f), "rb").read())
     except OSError:
         return None
@@ -147,7 +149,8 @@ def gpu_arm(args, rank, world, local_rank):
         wl = get_workload(args.workload, T=args.tokens_per_rank)
     W, T, D, F, k = wl.W, wl.T, wl.d_model, wl.d_ff, wl.topk
     inp = make_inputs(wl, device="cuda")
-    layer = ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas)
+    layer = ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas,
+                          producer_pairs=args.producer_pairs)
     sp = torch.cuda.Stream()
     sc = torch.cuda.Stream(priority=-1)
 
@@ -207,6 +210,7 @@ def gpu_arm(args, rank, world, local_rank):
     e2e = e2e_arm(layer, inp, wl, sp, sc, args)
 
     hbm, bf16, bf16_sus, src = _peaks()
+    launch = layer.launch_info()
     prod_avg = kernel_ms[2]
     achieved = flops_exec / (prod_avg * 1e-3) / 1e12
     result = {
@@ -225,12 +229,17 @@ def gpu_arm(args, rank, world, local_rank):
         "config": {"workload": wl.name, "W": W, "experts_per_rank": wl.L, "topk": k,
                    "tokens_per_rank": T, "d_model": D, "d_ff": F, "tb_M": wl.tb_M,
                    "mgb": wl.mgb, "consumer_ctas": args.consumer_ctas,
+                   "producer": "CTA pairs (cta_group::2, M=256)" if args.producer_pairs
+                   else "one CTA per tile (M=128)",
+                   "producer_ctas": launch[0], "consumer_ctas_launched": launch[1],
+                   "num_sms": launch[2], "pair_clusters_resident": launch[3],
                    "parallelism": f"{W} logical EP ranks on 1 GPU; replicas x{world}",
                    "l2": "inputs larger than L2: 768 MB of expert weights read every step"},
-        "roofline": {"kernel": "ffn_producer (GEMM1+SiLU+GEMM2, executed rows)",
+        "roofline": {"kernel": ("ffn_pair (CTA pairs, " if args.producer_pairs else "ffn_producer (")
+                     + "GEMM1+SiLU+GEMM2, executed rows)",
                      "bound": "tensor", "achieved": achieved, "peak": bf16_sus,
                      "unit": "TFLOP/s", "frac": achieved / bf16_sus,
-                     "traffic": producer_traffic(wl.name, args.tokens_per_rank),
+                     "traffic": producer_traffic(wl.name, args.tokens_per_rank, args.producer_pairs),
                      "peak_source": f"{src} bf16 sustained (kernel timed inside a loop of steps)",
                      "flops_per_launch": flops_exec, "launch_ms": prod_avg},
         "e2e": e2e,
@@ -269,9 +278,9 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=5):
     over = {n: statistics.median(v) for n, v in acc.items()}
     # serial mode: the producer on all SMs, then the consumer on all SMs with every flag set
     ser = {}
-    serial = capi.moe_cfg(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, 0, 0)
     from tile_signaled_grouped_gb300.runtime import ExpertCombine
-    lay2 = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, 0)
+    lay2 = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, 0,
+                         producer_pairs=args.producer_pairs)
     lay2.set_timing(True)
     for _ in range(iters):
         lay2.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
@@ -280,12 +289,12 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=5):
         for i, name in enumerate(["route", "plan", "producer", "consumer", "scale", "gather"]):
             ser.setdefault(name, []).append(t[i])
     ser = {n: statistics.median(v) for n, v in ser.items()}
-    del serial
     # Consumer CTAs beside the producer: whole-step time for a few partitions.
     sweep = {}
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for cc in [c for c in args.ccta_sweep if c >= 0]:
-        lay = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, cc)
+        lay = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, cc,
+                            producer_pairs=args.producer_pairs)
         for _ in range(3):
             lay.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
                         producer=sp, consumer=sc)
@@ -450,6 +459,8 @@ def main():
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--producer-pairs", type=int, default=1, choices=[0, 1],
+                    help="1: the CTA-pair producer (clusters of two, tcgen05 cta_group::2)")
     ap.add_argument("--ccta-sweep", type=lambda v: [int(x) for x in v.split(",") if x],
                     default=[0, 2, 4, 8, 16],
                     help="consumer-CTA counts whose step time is reported (outside the timed "

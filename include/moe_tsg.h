@@ -74,6 +74,11 @@ typedef struct moe_cfg {
                         0 = serial: the producer uses every SM, then the consumer runs
                         on every SM after it, on the producer stream. */
   long long timeout_ns; /* bound on every device-side wait; <= 0 selects 2 s */
+  int producer_pairs; /* 0: one producer CTA per 128-row tile (tcgen05.mma, M = 128).
+                         1: CTA pairs (clusters of two): each task covers two 128-row
+                         tiles of one expert, rows estart + 256 i and estart + 256 i + 128
+                         of its block, with one tcgen05.mma of M = 256 (cta_group::2);
+                         each CTA loads its own rows and half of the weight rows. */
 } moe_cfg;
 
 /* Opaque host-side handle; holds the configuration, the carved workspace
@@ -167,6 +172,18 @@ int moe_scale(moe_plan *plan, const float *topk_w, const void *const *recv, void
 int moe_plan_build_noalloc(const moe_cfg *cfg, const int32_t *topk_ids, void *plan_out,
                            size_t plan_out_bytes, moe_stream_t stream);
 
+/* How moe_expert_combine splits the GPU for this plan (pure host query; the
+ * occupancy is read once by moe_plan_create).
+ *  producer_ctas:   CTAs of one producer launch in the overlapped schedule (even
+ *                   with producer_pairs: clusters of two that fit on the GPU at once).
+ *  consumer_ctas:   CTAs of one consumer launch in the overlapped schedule.
+ *  num_sms:         SMs of the device.
+ *  pair_clusters:   clusters of two CTAs of the pair producer that fit on an idle
+ *                   GPU at once (0 if the runtime could not tell).
+ * Any output pointer may be NULL. */
+int moe_launch_info(moe_plan *plan, int *producer_ctas, int *consumer_ctas, int *num_sms,
+                    int *pair_clusters);
+
 /* Synchronises `stream` and reads the device status word: *code is 0 or a
  * MOE_DEV_* value, *detail the first failing item (token, band or tile index).
  * The status stays set until moe_status_clear(). */
@@ -196,13 +213,18 @@ enum moe_field {
   MOE_PLAN_SEG_NBANDS,       /* [W][NBmax] bands of each segment */
   MOE_PLAN_XSRC,             /* [W][RowsMax] per X row: source token s*T+t, or -1 */
   MOE_PLAN_SCALE_SRC,        /* [W][T][topk] >= 0: receive row; < 0: row -v-1 of own Y */
-  MOE_PLAN_TOTALS,           /* [8] 0: tiles, 1: segments, 2: tile units, 3: bands */
+  MOE_PLAN_TOTALS,           /* [8] 0: tiles, 1: segments, 2: tile units, 3: bands,
+                                4: consumer copy chunks, 5: producer CTA pairs */
   MOE_PLAN_TILE_ROW,         /* [tiles] per 128-row producer tile: rank*2^24 + first X row */
   MOE_PLAN_TILE_EXPERT,      /* [tiles] expert of each producer tile */
   MOE_PLAN_SEG_ORDER,        /* [segments] consumer order: rank*NBmax + segment */
   MOE_PLAN_STATUS,           /* [4] device status word */
   MOE_PLAN_FLAGS,            /* [W][NBmax][D/tile_N] ready flags of the last combine */
   MOE_PLAN_GROUP_SIG,        /* [W][W] group signals (sender, destination) of the last combine */
+  MOE_PLAN_PAIR,             /* [pairs][4] producer CTA pairs in pair order: the earlier tile of
+                                the tile order, its partner or -1, the earlier tile's
+                                rank*2^24 + first X row, and its local expert + 2^16 if the
+                                partner's rows lie 128 above */
   MOE_PLAN_NFIELDS,
   MOE_RANK_X = 100,          /* [RowsMax][D] bf16 expert input */
   MOE_RANK_H,                /* [RowsMax][F] bf16 hidden activation */

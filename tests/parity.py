@@ -50,10 +50,13 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().double().cpu().numpy()
 
 
-def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0):
-    """The whole path through the C ABI. mode: 'overlap' (two streams) or 'serial'."""
+def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0, pairs=0):
+    # pairs=0 keeps the one-CTA producer under test here; tests/test_gpu_pairs.py
+    # covers the pair producer.
+    """The whole path through the C ABI. mode: 'overlap' (two streams) or 'serial';
+    pairs: 1 runs the CTA-pair producer."""
     layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb,
-                          consumer_ctas if mode == "overlap" else 0, timeout_ns)
+                          consumer_ctas if mode == "overlap" else 0, timeout_ns, pairs)
     sp = torch.cuda.Stream()
     sc = torch.cuda.Stream(priority=-1)
     torch.cuda.synchronize()
@@ -138,6 +141,34 @@ def check_order(layer, wl, plan):
     nbm = g(capi.MOE_PLAN_SCHEDULE).size // wl.W
     assert sorted(so.tolist()) == sorted(o * nbm + j for o in range(wl.W)
                                          for j in range(len(plan.segments[o])))
+
+
+def check_pairs(layer, wl, plan):
+    """The CTA-pair list, which is unique: tiles j and j^1 of one expert's block
+    (rows expert_start + 128 j) form a pair, listed at the earlier of the two tile
+    positions, the earlier tile first; a tile whose partner lies past the block
+    is alone (partner -1)."""
+    g = lambda f: layer.field(f).cpu().numpy()
+    tot = g(capi.MOE_PLAN_TOTALS)
+    ntiles, npairs = int(tot[0]), int(tot[5])
+    tr = g(capi.MOE_PLAN_TILE_ROW)[:ntiles]
+    te = g(capi.MOE_PLAN_TILE_EXPERT)[:ntiles]
+    groups = {}
+    for pos in range(ntiles):
+        o, row, e = int(tr[pos]) >> 24, int(tr[pos]) & 0xFFFFFF, int(te[pos])
+        assert e // wl.L == o
+        j = (row - int(plan.expert_start[e])) // 128
+        groups.setdefault((e, j // 2), []).append(pos)
+    want = sorted((sorted(v) + [-1])[:2] for v in groups.values())
+    rec = g(capi.MOE_PLAN_PAIR)[:4 * npairs].reshape(-1, 4)
+    assert npairs == len(want), (npairs, len(want))
+    assert rec[:, :2].tolist() == want, "pair list"
+    for first, second, trow, info in rec.tolist():
+        assert trow == int(tr[first]), "pair record: rank and row"
+        assert info & 0xFFFF == int(te[first]) % wl.L, "pair record: local expert"
+        if second >= 0:
+            above = (int(tr[second]) & 0xFFFFFF) < (trow & 0xFFFFFF)
+            assert bool(info >> 16) == above, "pair record: partner side"
 
 
 def check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=None, rng=None):

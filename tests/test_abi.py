@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def _cfg(**kw):
     base = dict(W=4, L=2, topk=2, T=4096, d_model=2048, d_ff=8192, tb_M=128, mgb=1,
-                consumer_ctas=8, timeout_ns=0)
+                consumer_ctas=8, timeout_ns=0, producer_pairs=0)
     base.update(kw)
     return capi.moe_cfg(*[base[f] for f, _ in capi.moe_cfg._fields_])
 
@@ -69,10 +69,20 @@ def test_workspace_sizes_follow_the_worst_case(lib):
 @pytest.mark.parametrize("bad", [
     dict(W=0), dict(W=9), dict(L=0), dict(topk=0), dict(topk=9, W=1, L=8), dict(T=0),
     dict(d_model=100), dict(d_ff=64), dict(tb_M=96), dict(mgb=0), dict(consumer_ctas=-1),
+    dict(producer_pairs=2), dict(producer_pairs=-1),
 ])
 def test_invalid_configurations_are_rejected(lib, bad):
     with pytest.raises(capi.MoeError, match="MOE_ERR_ARG"):
         capi.moe_workspace_size(_cfg(**bad))
+
+
+def test_cfg_struct_matches_the_header(lib):
+    """The ctypes mirror of moe_cfg has the header's fields in the header's order."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct moe_cfg \{(.*?)\} moe_cfg;", text, re.S).group(1)
+    names = re.findall(r"(\w+);", body)
+    assert names == [f for f, _ in capi.moe_cfg._fields_]
+    assert ctypes.sizeof(capi.moe_cfg) == 56
 
 
 def test_host_errors_without_a_device(lib):

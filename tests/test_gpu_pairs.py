@@ -1,0 +1,107 @@
+"""Parity of the CTA-pair producer (clusters of two CTAs, one tcgen05.mma of
+M = 256 over two 128-row tiles of one expert) against the CPU oracle, through
+the C ABI: the same checks as the one-CTA producer's parity tests, plus the
+pair list itself (unique, so compared exactly)."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+from tests import parity as P  # noqa: E402
+from tests.test_gpu_parity import FULL, SMALL  # noqa: E402
+from tile_signaled_grouped_gb300 import capi  # noqa: E402
+from tile_signaled_grouped_gb300.workloads import Workload, get_workload  # noqa: E402
+
+
+def _full_check(wl, mode="overlap", cctas=8):
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode=mode, consumer_ctas=cctas, pairs=1)
+    assert layer.status() == (0, 0)
+    ids, w, plan = P.oracle_plan(wl, inp)
+    P.check_plan(layer, wl, plan, ids, w)
+    P.check_order(layer, wl, plan)
+    P.check_pairs(layer, wl, plan)
+    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w)
+    layer.close()
+
+
+@pytest.mark.parametrize("mode", ["serial", "overlap"])
+@pytest.mark.parametrize("mgb", [1, 2])
+def test_pairs_tiny_full_parity(mode, mgb):
+    _full_check(get_workload("tiny", mgb=mgb), mode)
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_pairs_small_shapes_full_parity(wl):
+    _full_check(wl, "overlap", cctas=4)
+
+
+def test_pairs_odd_tile_counts():
+    """Experts whose blocks hold an odd number of 128-row tiles leave one tile
+    without a partner; its CTA's rows are computed and discarded."""
+    # tiles per expert: 4, 3, 2, 2, 1, 1
+    wl = Workload("odd_tiles", W=2, L=3, topk=2, T=333, d_model=256, d_ff=256, tb_M=64,
+                  routing="zipf")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="serial", pairs=1)
+    assert layer.status() == (0, 0)
+    ids, w, plan = P.oracle_plan(wl, inp)
+    npairs = int(layer.field(capi.MOE_PLAN_TOTALS)[5])
+    pr = layer.field(capi.MOE_PLAN_PAIR)[:4 * npairs].view(-1, 4)
+    assert (pr[:, 1] < 0).any(), "the shape should leave a tile alone"
+    P.check_pairs(layer, wl, plan)
+    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_pairs_full_size_sampled(name):
+    wl = get_workload(name)
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="overlap", consumer_ctas=4, pairs=1)
+    assert layer.status() == (0, 0)
+    ids, w, plan = P.oracle_plan(wl, inp)
+    P.check_plan(layer, wl, plan, ids, w)
+    P.check_pairs(layer, wl, plan)
+    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=12,
+                               rng=np.random.default_rng(1))
+
+
+def test_pairs_match_one_cta_producer_bit_for_bit():
+    """Both producers accumulate each output element over K in the same order of
+    16-wide MMA steps, so h, Y and the outputs are identical."""
+    wl = SMALL[0]
+    inp = P.inputs_for(wl)
+    one = P.run_gpu(wl, inp, mode="serial", pairs=0)
+    two = P.run_gpu(wl, inp, mode="serial", pairs=1)
+    assert one.status() == (0, 0) and two.status() == (0, 0)
+    rows = one.field(capi.MOE_PLAN_RANK_ROWS).tolist()
+    for o in range(wl.W):
+        for f in (capi.MOE_RANK_H, capi.MOE_RANK_Y):
+            a, b = one.rank_field(f, o)[:rows[o]], two.rank_field(f, o)[:rows[o]]
+            assert torch.equal(a, b), (o, f, (a.float() - b.float()).abs().max().item())
+    for a, b in zip(one.out, two.out):
+        assert torch.equal(a, b)
+
+
+def test_pairs_repeat_runs_are_identical():
+    wl = get_workload("tiny")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, pairs=1)
+    out0 = [t.clone() for t in layer.out]
+    for _ in range(5):
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(out0, layer.out))
+    assert layer.status() == (0, 0)
+
+
+def test_pairs_device_wait_timeout_is_reported_and_recoverable():
+    wl = get_workload("a100_like")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, timeout_ns=20_000, pairs=1)
+    code, _ = layer.status()
+    assert code == capi.MOE_DEV_TIMEOUT
+    layer.close()
+    layer = P.run_gpu(wl, inp, pairs=1)
+    assert layer.status() == (0, 0)

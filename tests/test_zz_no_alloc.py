@@ -53,7 +53,8 @@ def test_noalloc_plan_equals_plan_build_on_two_calls_in_a_row(name):
             if f in ("MOE_PLAN_BAND_EXPERT", "MOE_PLAN_BAND_DST", "MOE_PLAN_BAND_VALID",
                      "MOE_PLAN_BAND_DST_ROW", "MOE_PLAN_SCHEDULE", "MOE_PLAN_SEG_FIRST",
                      "MOE_PLAN_SEG_NBANDS", "MOE_PLAN_XSRC", "MOE_PLAN_TILE_ROW",
-                     "MOE_PLAN_TILE_EXPERT", "MOE_PLAN_SEG_ORDER", "MOE_PLAN_TOTALS"):
+                     "MOE_PLAN_TILE_EXPERT", "MOE_PLAN_SEG_ORDER", "MOE_PLAN_TOTALS",
+                     "MOE_PLAN_PAIR"):
                 continue
             assert torch.equal(got, want), f"call {call}: {f}"
         _compare_prefixes(ref, out, wl_call)
@@ -81,9 +82,9 @@ def _compare_prefixes(ref, out, wl):
             b = ref.field(capi.ENUMS[f])[o * stride:o * stride + n]
             assert torch.equal(a, b), f"{f} of rank {o}"
     tot = ref.field(capi.MOE_PLAN_TOTALS).tolist()
-    assert view("MOE_PLAN_TOTALS")[:5].tolist() == tot[:5]
+    assert view("MOE_PLAN_TOTALS")[:6].tolist() == tot[:6]
     for f, n in [("MOE_PLAN_TILE_ROW", tot[0]), ("MOE_PLAN_TILE_EXPERT", tot[0]),
-                 ("MOE_PLAN_SEG_ORDER", tot[1])]:
+                 ("MOE_PLAN_SEG_ORDER", tot[1]), ("MOE_PLAN_PAIR", 4 * tot[5])]:
         assert torch.equal(view(f)[:n], ref.field(capi.ENUMS[f])[:n]), f
 
 

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_tsg.so")
-SOURCES = ["api.cu", "plan.cu", "ffn.cu", "consumer.cu", "route_scale.cu", "plan_noalloc.cu"]
+SOURCES = ["api.cu", "plan.cu", "ffn.cu", "ffn_pair.cu", "consumer.cu", "route_scale.cu",
+           "plan_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

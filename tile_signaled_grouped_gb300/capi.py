@@ -33,6 +33,7 @@ class moe_cfg(ctypes.Structure):
         ("mgb", ctypes.c_int),
         ("consumer_ctas", ctypes.c_int),
         ("timeout_ns", ctypes.c_longlong),
+        ("producer_pairs", ctypes.c_int),
     ]
 
 
@@ -82,6 +83,7 @@ def load():
         "moe_set_timing": (ip, [vp, ip]),
         "moe_timings": (ip, [vp, P(ctypes.c_float), ip]),
         "moe_plan_build_noalloc": (ip, [P(moe_cfg), vp, vp, sz, vp]),
+        "moe_launch_info": (ip, [vp, P(ip), P(ip), P(ip), P(ip)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -180,3 +182,10 @@ def moe_timings(plan, n: int = 6):
 def moe_plan_build_noalloc(cfg: moe_cfg, topk_ids, plan_out, plan_out_bytes, stream):
     check(lib().moe_plan_build_noalloc(ctypes.byref(cfg), topk_ids, plan_out, plan_out_bytes,
                                        stream), "moe_plan_build_noalloc")
+
+
+def moe_launch_info(plan):
+    """(producer_ctas, consumer_ctas, num_sms, pair_clusters) of the overlapped schedule."""
+    v = [ctypes.c_int() for _ in range(4)]
+    check(lib().moe_launch_info(plan, *[ctypes.byref(x) for x in v]), "moe_launch_info")
+    return tuple(x.value for x in v)

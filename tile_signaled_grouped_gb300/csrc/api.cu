@@ -31,6 +31,7 @@ struct moe_plan {
   size_t counts[PA_COUNT];
   RankLayout rl;
   int num_sms;
+  int pair_clusters;  // CTA pairs of the pair producer resident at once (0: unknown)
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   cudaEvent_t ev_ready, ev_join;
   cudaEvent_t ev_t0[kTSlots][kTRing], ev_t1[kTSlots][kTRing];
@@ -50,6 +51,7 @@ int dims_from_cfg(const moe_cfg* c, Dims* d) {
   if (c->d_model > 16384 || c->d_ff > 65536) return MOE_ERR_UNSUPPORTED;  // a row fits one copy chunk
   if (c->tb_M != 64 && c->tb_M != 128 && c->tb_M != 256) return MOE_ERR_ARG;
   if (c->mgb < 1 || c->consumer_ctas < 0) return MOE_ERR_ARG;
+  if (c->producer_pairs != 0 && c->producer_pairs != 1) return MOE_ERR_ARG;
   Dims x{};
   x.W = c->W;
   x.L = c->L;
@@ -110,6 +112,8 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_GROUP_NCHUNK] = W * W;
   n[PA_XSRC] = W * (size_t)d.RM;
   n[PA_SCALE_SRC] = W * (size_t)d.T * d.k;
+  n[PA_PAIR] = 4 * W * NMM;
+  n[PA_PAIR_UNIT_BEGIN] = n[PA_UNIT_BEGIN];
   size_t pos = 0;
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;
@@ -149,6 +153,25 @@ DevPlan dev_plan(const moe_plan* p) {
     dp.a[i] = reinterpret_cast<int32_t*>(p->plan_ws + p->offsets[i]);
   dp.timeout_ns = p->cfg.timeout_ns > 0 ? p->cfg.timeout_ns : 2000000000LL;
   return dp;
+}
+
+struct LaunchShape {
+  int producer, consumer;
+};
+
+// Grids of the producer and the consumer. Overlapped: the consumer's CTAs and the
+// producer's share the SMs (one CTA of either per SM). The pair producer's grid
+// also stops at the clusters that fit at once: the others would only start once
+// the rest had finished.
+LaunchShape launch_shape(const moe_plan* p, bool serial) {
+  LaunchShape ls{};
+  ls.consumer = serial ? p->num_sms : p->cfg.consumer_ctas;
+  ls.producer = serial ? p->num_sms : p->num_sms - p->cfg.consumer_ctas;
+  if (p->cfg.producer_pairs) {
+    if (p->pair_clusters > 0) ls.producer = std::min(ls.producer, 2 * p->pair_clusters);
+    ls.producer = std::max(2, ls.producer & ~1);
+  }
+  return ls;
 }
 
 bool aligned16(const void* ptr) { return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
@@ -210,7 +233,7 @@ int moe_field(const moe_cfg* cfg, int field, size_t* byte_offset, size_t* count)
       PA_BAND_EXPERT,  PA_BAND_DST,    PA_BAND_VALID, PA_BAND_DST_ROW, PA_SCHED,
       PA_SEG_FIRST,    PA_SEG_NB,      PA_XSRC,       PA_SCALE_SRC,    PA_TOTALS,
       PA_TILE_ROW,     PA_TILE_EXPERT, PA_SEG_ORDER,  PA_STATUS,       PA_FLAGS,
-      PA_GROUP_SIG};
+      PA_GROUP_SIG,    PA_PAIR};
   if (field < 0 || field >= MOE_PLAN_NFIELDS) return MOE_ERR_ARG;
   size_t off[PA_COUNT], cnt[PA_COUNT];
   plan_layout(d, off, cnt);
@@ -240,7 +263,8 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
     return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;
 
-  if (preload_producer() != cudaSuccess || preload_consumer() != cudaSuccess ||
+  if (preload_producer() != cudaSuccess || preload_producer_pair() != cudaSuccess ||
+      preload_consumer() != cudaSuccess ||
       preload_plan() != cudaSuccess || preload_route_scale() != cudaSuccess)
     return MOE_ERR_CUDA;
 
@@ -261,6 +285,7 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
   std::memcpy(p->counts, cnt, sizeof(cnt));
   p->rl = rl;
   p->num_sms = prop.multiProcessorCount;
+  p->pair_clusters = producer_pair_max_clusters();
   p->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   bool ok = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) == cudaSuccess;
@@ -334,8 +359,9 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
   cudaStream_t sp = reinterpret_cast<cudaStream_t>(producer);
   cudaStream_t sc = reinterpret_cast<cudaStream_t>(consumer);
   const bool serial = p->cfg.consumer_ctas == 0 || sp == sc;
-  const int cgrid = serial ? p->num_sms : p->cfg.consumer_ctas;
-  const int pgrid = serial ? p->num_sms : p->num_sms - p->cfg.consumer_ctas;
+  const bool pairs = p->cfg.producer_pairs != 0;
+  const LaunchShape ls = launch_shape(p, serial);
+  const int cgrid = ls.consumer, pgrid = ls.producer;
 
   ProducerArgs pa;
   std::memset(&pa, 0, sizeof(pa));
@@ -349,13 +375,17 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
         !make_map(p, &pa.tm_h[r], H, d.RM, d.F, kTileM) ||
         !make_map(p, &pa.tm_wg[r], w_gate[r], (uint64_t)d.L * d.F, d.D, kN1) ||
         !make_map(p, &pa.tm_wu[r], w_up[r], (uint64_t)d.L * d.F, d.D, kN1) ||
-        !make_map(p, &pa.tm_wd[r], w_down[r], (uint64_t)d.L * d.D, d.F, d.N2))
+        !make_map(p, &pa.tm_wd[r], w_down[r], (uint64_t)d.L * d.D, d.F, pairs ? d.N2 / 2 : d.N2))
       return MOE_ERR_ARG;
     pa.h[r] = H;
     pa.y[r] = Y;
   }
-  const int per_unit = kTileGroup * (d.nt1 + d.nt2);
-  pa.lag = (2 * pgrid + per_unit - 1) / per_unit + 1;
+  // GEMM2 tasks of a unit start `lag` units after its GEMM1 tasks: about two
+  // tasks per CTA (or CTA pair) in flight separate them. A pair unit holds about
+  // half as many tasks as a tile unit.
+  const int workers = pairs ? pgrid / 2 : pgrid;
+  const int per_unit = (pairs ? kTileGroup / 2 : kTileGroup) * (d.nt1 + d.nt2);
+  pa.lag = (2 * workers + per_unit - 1) / per_unit + 1;
 
   ConsumerArgs ca;
   std::memset(&ca, 0, sizeof(ca));
@@ -371,7 +401,7 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
   CUDA_TRY(cudaMemsetAsync(p->plan_ws + z0, 0, z1 - z0, sp));
   if (serial) {
     tstart(p, kTProducer, sp);
-    CUDA_TRY(launch_producer(pa, pgrid, sp));
+    CUDA_TRY(pairs ? launch_producer_pair(pa, pgrid, sp) : launch_producer(pa, pgrid, sp));
     tstop(p, kTProducer, sp);
     tstart(p, kTConsumer, sp);
     CUDA_TRY(launch_consumer(ca, cgrid, sp));
@@ -384,7 +414,7 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
     tstop(p, kTConsumer, sc);
     CUDA_TRY(cudaEventRecord(p->ev_join, sc));
     tstart(p, kTProducer, sp);
-    CUDA_TRY(launch_producer(pa, pgrid, sp));
+    CUDA_TRY(pairs ? launch_producer_pair(pa, pgrid, sp) : launch_producer(pa, pgrid, sp));
     tstop(p, kTProducer, sp);
     CUDA_TRY(cudaStreamWaitEvent(sp, p->ev_join, 0));
   }
@@ -409,6 +439,17 @@ int moe_scale(moe_plan* p, const float* topk_w, const void* const* recv, void* c
   tstart(p, kTScale, s);
   CUDA_TRY(launch_scale(a, p->num_sms, s));
   tstop(p, kTScale, s);
+  return MOE_OK;
+}
+
+int moe_launch_info(moe_plan* p, int* producer_ctas, int* consumer_ctas, int* num_sms,
+                    int* pair_clusters) {
+  if (p == nullptr) return MOE_ERR_ARG;
+  const LaunchShape ls = launch_shape(p, false);
+  if (producer_ctas) *producer_ctas = ls.producer;
+  if (consumer_ctas) *consumer_ctas = ls.consumer;
+  if (num_sms) *num_sms = p->num_sms;
+  if (pair_clusters) *pair_clusters = p->pair_clusters;
   return MOE_OK;
 }
 

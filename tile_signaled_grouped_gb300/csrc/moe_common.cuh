@@ -63,6 +63,7 @@ enum PlanArray {
   PA_RANK_TILES, PA_TILE_ROW, PA_TILE_EXPERT, PA_UNIT_BEGIN, PA_SEG_ORDER,
   PA_SEG_REC, PA_GROUP_NCHUNK,
   PA_XSRC, PA_SCALE_SRC,
+  PA_PAIR, PA_PAIR_UNIT_BEGIN,
   PA_COUNT
 };
 
@@ -117,6 +118,11 @@ struct ProducerArgs {
   int lag;  // scheduling units between a unit's GEMM1 tiles and its GEMM2 tiles
 };
 cudaError_t launch_producer(const ProducerArgs& a, int grid, cudaStream_t s);
+// CTA-pair producer (clusters of two, tcgen05 cta_group::2); grid is rounded down
+// to an even count. Its tm_wd maps use boxes of N2/2 rows.
+cudaError_t preload_producer_pair();
+int producer_pair_max_clusters();  // clusters of two resident at once on an idle GPU (0: unknown)
+cudaError_t launch_producer_pair(const ProducerArgs& a, int grid, cudaStream_t s);
 
 struct ConsumerArgs {
   const __nv_bfloat16* y[MOE_MAX_RANKS];

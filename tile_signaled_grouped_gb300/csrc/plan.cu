@@ -457,6 +457,50 @@ __global__ void __launch_bounds__(1024) plan_order_kernel(DevPlan p) {
   }
   __syncthreads();
 
+  // 2b. CTA pairs of the pair producer: tiles j and j^1 of one expert (rows
+  // estart + 128 j of its block) form a pair, listed where the earlier of the
+  // two sits in the tile order, as one 16-byte record. The pair units are the
+  // tile units: unit u holds the pairs whose earlier tile lies in tile unit u.
+  {
+    int32_t* heads_before = rank_tiles;  // reuse: pairs listed before each tile position
+    int carry_p = 0;
+    for (int base = 0; base < NM; base += nt) {
+      const int pos = base + tid;
+      int partner = -1;
+      bool head = false;
+      int4 rec;
+      if (pos < NM) {
+        const int tr = p.a[PA_TILE_ROW][pos];
+        const int o = tr >> 24, row = tr & 0xFFFFFF;
+        const int e = p.a[PA_TILE_EXPERT][pos];
+        const int es = p.a[PA_EXPERT_START][e], ra = p.a[PA_ROWS_ALLOC][e];
+        const int prow = es + (((row - es) / kTileM) ^ 1) * kTileM;
+        if (prow < es + ra)
+          partner = p.a[PA_BAND_TILE][(size_t)o * d.NBM + prow / tb] +
+                    (tb > kTileM ? (prow % tb) / kTileM : 0);
+        head = partner < 0 || pos < partner;
+        // Record of the pair: first tile, partner, first tile's (rank, row), and
+        // the local expert with one bit saying whether the partner's rows lie
+        // 128 above (else 128 below) the first tile's.
+        rec = make_int4(pos, partner, tr, (e - o * d.L) | (partner >= 0 && prow < row ? 1 << 16 : 0));
+      }
+      int tot;
+      const int idx = carry_p + block_excl_scan(head ? 1 : 0, scratch, &tot);
+      if (pos < NM) {
+        heads_before[pos] = idx;
+        if (head) reinterpret_cast<int4*>(p.a[PA_PAIR])[idx] = rec;
+      }
+      carry_p += tot;
+    }
+    __syncthreads();
+    for (int u = tid; u <= NU; u += nt) {
+      const int b = p.a[PA_UNIT_BEGIN][u];
+      p.a[PA_PAIR_UNIT_BEGIN][u] = b < NM ? heads_before[b] : carry_p;
+    }
+    if (tid == 0) p.a[PA_TOTALS][5] = carry_p;
+    __syncthreads();
+  }
+
   // 3. Consumer order: segments sorted by the tile of their first band.
   int32_t* slot = p.a[PA_RANK_TILES];  // reuse: [2 * NM] slots, -1 = empty
   __syncthreads();

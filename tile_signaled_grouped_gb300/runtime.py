@@ -21,10 +21,10 @@ class ExpertCombine:
     """One MoE layer split over W logical ranks on the current CUDA device."""
 
     def __init__(self, W, L, topk, T, d_model, d_ff, tb_M, mgb=1, consumer_ctas=8,
-                 timeout_ns=0, device=None):
+                 timeout_ns=0, producer_pairs=1, device=None):
         self.device = torch.device(device or "cuda")
         self.cfg = capi.moe_cfg(W, L, topk, T, d_model, d_ff, tb_M, mgb, consumer_ctas,
-                                timeout_ns)
+                                timeout_ns, producer_pairs)
         self.W, self.L, self.k, self.T, self.D, self.F = W, L, topk, T, d_model, d_ff
         plan_bytes, rank_bytes, recv_rows = capi.moe_workspace_size(self.cfg)
         self.plan_bytes, self.rank_bytes, self.recv_rows = plan_bytes, rank_bytes, recv_rows
@@ -106,6 +106,10 @@ class ExpertCombine:
         off, cnt = capi.moe_field(self.cfg, field)
         cols = self.F if field == capi.MOE_RANK_H else self.D
         return self.rank_ws[rank][off:off + 2 * cnt].view(torch.bfloat16).view(-1, cols)
+
+    def launch_info(self):
+        """(producer_ctas, consumer_ctas, num_sms, pair_clusters) of the overlapped schedule."""
+        return capi.moe_launch_info(self.plan)
 
     def set_timing(self, enable=True):
         capi.moe_set_timing(self.plan, enable)
