@@ -81,46 +81,70 @@ __global__ void route_kernel(DevPlan p, const float* __restrict__ logits,
 }
 
 // One warp per token (s, t): out_s[t] = sum_j w_j * row_j, fp32 in slot order.
-// The lanes fetch the token's scale-map entries and weights once (one round
-// trip), then each lane covers two 16-byte chunks of every row per pass, so a
-// warp keeps 2k independent 16-byte loads per lane in flight.
+// Lane j < k holds slot j's source (scale map) and weight; the next token's are
+// fetched while the current token is summed. Each lane covers two 16-byte chunks
+// of the row per pass and gathers up to four slots' chunks into registers before
+// accumulating, so a lane keeps up to eight independent 16-byte loads in flight.
+// Slot order of the fp32 sum is kept (j ascending).
+constexpr int kScaleGroup = 4;
+
+__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(h[q]);
+    acc[2 * q] = fmaf(w, f.x, acc[2 * q]);
+    acc[2 * q + 1] = fmaf(w, f.y, acc[2 * q + 1]);
+  }
+}
+
 __global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
   const int lane = threadIdx.x & 31;
   const int n16 = d.D / 8;
+  const int ntok = d.W * d.T;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < d.W * d.T; tok += warps) {
-    const int s = tok / d.T, t = tok % d.T;
-    int src_l = INT_MIN;
-    float w_l = 0.f;
-    if (lane < d.k) {
-      src_l = a.p.a[PA_SCALE_SRC][(size_t)tok * d.k + lane];
-      w_l = a.w[(size_t)tok * d.k + lane];
+  int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int src_n = INT_MIN;
+  float w_n = 0.f;
+  if (tok < ntok && lane < d.k) {
+    src_n = __ldg(a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k + lane);
+    w_n = __ldg(a.w + (size_t)tok * d.k + lane);
+  }
+  for (; tok < ntok; tok += warps) {
+    const int src_l = src_n;
+    const float w_l = w_n;
+    const int nxt = tok + warps;
+    if (nxt < ntok && lane < d.k) {
+      src_n = __ldg(a.p.a[PA_SCALE_SRC] + (size_t)nxt * d.k + lane);
+      w_n = __ldg(a.w + (size_t)nxt * d.k + lane);
     }
+    const int s = tok / d.T, t = tok % d.T;
     uint4* out = reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D);
     for (int c0 = 0; c0 < n16; c0 += 64) {
       const int ca = c0 + lane, cb = c0 + 32 + lane;
       float acc0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       float acc1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int j = 0; j < d.k; ++j) {
-        const int sj = __shfl_sync(0xffffffffu, src_l, j);
-        const float wj = __shfl_sync(0xffffffffu, w_l, j);
-        if (sj == INT_MIN) continue;  // invalid routing slot (reported by the plan)
-        const uint4* row = reinterpret_cast<const uint4*>(
-            sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D);
-        const uint4 va = ca < n16 ? __ldg(row + ca) : make_uint4(0, 0, 0, 0);
-        const uint4 vb = cb < n16 ? __ldg(row + cb) : make_uint4(0, 0, 0, 0);
-        const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&va);
-        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&vb);
+      for (int j0 = 0; j0 < d.k; j0 += kScaleGroup) {
+        uint4 va[kScaleGroup], vb[kScaleGroup];
+        float wj[kScaleGroup];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 fa = __bfloat1622float2(ha[q]);
-          const float2 fb = __bfloat1622float2(hb[q]);
-          acc0[2 * q] = fmaf(wj, fa.x, acc0[2 * q]);
-          acc0[2 * q + 1] = fmaf(wj, fa.y, acc0[2 * q + 1]);
-          acc1[2 * q] = fmaf(wj, fb.x, acc1[2 * q]);
-          acc1[2 * q + 1] = fmaf(wj, fb.y, acc1[2 * q + 1]);
+        for (int q = 0; q < kScaleGroup; ++q) {
+          const int j = j0 + q;
+          const int sj = __shfl_sync(0xffffffffu, src_l, j & 31);
+          wj[q] = __shfl_sync(0xffffffffu, w_l, j & 31);
+          // Slots past k, and invalid routing slots (reported by the plan), add nothing.
+          const bool live = j < d.k && sj != INT_MIN;
+          if (!live) wj[q] = 0.f;
+          const uint4* row = reinterpret_cast<const uint4*>(
+              sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D);
+          va[q] = live && ca < n16 ? __ldg(row + ca) : make_uint4(0, 0, 0, 0);
+          vb[q] = live && cb < n16 ? __ldg(row + cb) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < kScaleGroup; ++q) {
+          fma_bf16x8(acc0, wj[q], va[q]);
+          fma_bf16x8(acc1, wj[q], vb[q]);
         }
       }
       if (ca < n16)
@@ -135,11 +159,20 @@ __global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ Scal
 
 }  // namespace
 
+namespace {
+int g_scale_blocks_per_sm = 0;  // resident scale blocks per SM (set at preload)
+}
+
 cudaError_t preload_route_scale() {
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, route_kernel);
   if (e != cudaSuccess) return e;
-  return cudaFuncGetAttributes(&fa, scale_kernel);
+  if ((e = cudaFuncGetAttributes(&fa, scale_kernel)) != cudaSuccess) return e;
+  int n = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scale_kernel, 256, 0)) != cudaSuccess)
+    return e;
+  g_scale_blocks_per_sm = n;
+  return cudaSuccess;
 }
 
 cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* forced,
@@ -150,9 +183,11 @@ cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* f
 }
 
 cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s) {
-  // Eight warps per block, up to 16 blocks per SM: one token per warp at a time.
+  // Eight warps per block, one token per warp at a time; as many blocks as fit on
+  // the GPU at once, so every warp walks several tokens (and prefetches the next).
   const int tokens = a.p.d.W * a.p.d.T;
-  const int blocks = std::min((tokens + 7) / 8, num_sms * 16);
+  const int per_sm = g_scale_blocks_per_sm > 0 ? g_scale_blocks_per_sm : 4;
+  const int blocks = std::min((tokens + 7) / 8, num_sms * per_sm);
   scale_kernel<<<blocks, 256, 0, s>>>(a);
   return cudaGetLastError();
 }

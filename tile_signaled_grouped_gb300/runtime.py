@@ -76,19 +76,24 @@ class ExpertCombine:
                                 [t.data_ptr() for t in w_up], [t.data_ptr() for t in w_down],
                                 [t.data_ptr() for t in self.recv], sp, sc)
 
-    def scale(self, w=None, stream=None):
+    def scale(self, w=None, stream=None, out=None):
+        """out: W tensors [T, D] bf16 to write (default: the layer's own outputs)."""
         w = self.w if w is None else w
+        out = self.out if out is None else out
         capi.moe_scale(self.plan, w.data_ptr(), [t.data_ptr() for t in self.recv],
-                       [t.data_ptr() for t in self.out], _stream_handle(stream))
-        return self.out
+                       [t.data_ptr() for t in out], _stream_handle(stream))
+        return out
 
     def forward(self, x, w_gate, w_up, w_down, logits, forced_ids=None, producer=None,
-                consumer=None):
-        """route -> plan -> overlapped FFN and combine -> scale; all on the GPU."""
+                consumer=None, out=None):
+        """route -> plan -> overlapped FFN and combine -> scale; all on the GPU.
+
+        Every call is enqueued on `producer` (and `consumer`): inputs written on
+        another stream must be complete before it (an event or a synchronize)."""
         self.route(logits, forced_ids, producer)
         self.plan_build(x, stream=producer)
         self.expert_combine(w_gate, w_up, w_down, producer, consumer)
-        return self.scale(stream=producer)
+        return self.scale(stream=producer, out=out)
 
     # ------------------------------------------------------------- inspection
     def status(self, stream=None):
@@ -116,3 +121,76 @@ class ExpertCombine:
 
     def timings(self):
         return capi.moe_timings(self.plan, 6)
+
+
+class HostPipeline:
+    """Steps of one layer fed from and returned to pinned host memory, with the copies
+    overlapped with compute: step i+1's inputs are copied in while step i computes,
+    and step i's outputs are copied out while step i+1 computes.
+
+    Two sets of device inputs (tokens, logits, forced ids) and two sets of outputs
+    alternate; one copy stream per direction. Events order everything on the GPU:
+    a set's inputs are overwritten only after the plan build of the step that read
+    them, and its outputs only after their copy to the host finished. Every step
+    still moves all of its input and output bytes; nothing is cached across steps.
+    """
+
+    def __init__(self, layer: ExpertCombine, producer=None, consumer=None, forced=False):
+        dev = layer.device
+        W, T, D, E, k = layer.W, layer.T, layer.D, layer.W * layer.L, layer.k
+        self.layer = layer
+        self.sp = producer or torch.cuda.Stream(device=dev)
+        self.sc = consumer or torch.cuda.Stream(device=dev, priority=-1)
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.x = [[torch.empty(T, D, dtype=torch.bfloat16, device=dev) for _ in range(W)]
+                  for _ in range(2)]
+        self.logits = [torch.empty(W, T, E, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.forced = [torch.empty(W, T, k, dtype=torch.int32, device=dev) if forced else None
+                       for _ in range(2)]
+        self.out = [[torch.empty(T, D, dtype=torch.bfloat16, device=dev) for _ in range(W)]
+                    for _ in range(2)]
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.ev_in, self.ev_free, self.ev_done, self.ev_out = ev(), ev(), ev(), ev()
+        self.started = [False, False]
+        self.i = 0
+
+    def step(self, hx, hlogits, hforced, hout, w_gate, w_up, w_down, start_after=None):
+        """Enqueue one step. hx: W pinned [T, D] bf16; hlogits: pinned [W, T, E] fp32;
+        hforced: pinned [W, T, k] int32 or None; hout: W pinned [T, D] bf16 written when
+        the step's output copy completes (after self.done_event() of this step).
+        start_after: an event the first copy must follow (for timing)."""
+        b = self.i % 2
+        lay = self.layer
+        if start_after is not None:
+            self.s_in.wait_event(start_after)
+        if self.started[b]:
+            self.s_in.wait_event(self.ev_free[b])
+        with torch.cuda.stream(self.s_in):
+            for d, h in zip(self.x[b], hx):
+                d.copy_(h, non_blocking=True)
+            self.logits[b].copy_(hlogits, non_blocking=True)
+            if hforced is not None:
+                self.forced[b].copy_(hforced, non_blocking=True)
+        self.ev_in[b].record(self.s_in)
+        self.sp.wait_event(self.ev_in[b])
+        lay.route(self.logits[b], self.forced[b] if hforced is not None else None, self.sp)
+        lay.plan_build(self.x[b], stream=self.sp)
+        self.ev_free[b].record(self.sp)
+        lay.expert_combine(w_gate, w_up, w_down, self.sp, self.sc)
+        if self.started[b]:
+            self.sp.wait_event(self.ev_out[b])
+        lay.scale(stream=self.sp, out=self.out[b])
+        self.ev_done[b].record(self.sp)
+        self.s_out.wait_event(self.ev_done[b])
+        with torch.cuda.stream(self.s_out):
+            for h, o in zip(hout, self.out[b]):
+                h.copy_(o, non_blocking=True)
+        self.ev_out[b].record(self.s_out)
+        self.started[b] = True
+        self.i += 1
+        return self.ev_out[b]
+
+    def done_event(self):
+        """Event completed when the last enqueued step's outputs are on the host."""
+        return self.ev_out[(self.i - 1) % 2]
