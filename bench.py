@@ -260,7 +260,7 @@ def gpu_arm(args, rank, world, local_rank):
     return result
 
 
-def stage_times(layer, inp, wl, sp, sc, args, iters=5):
+def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     """Per-kernel times of one step, and the producer alone on every SM (serial mode)."""
     import torch
 

@@ -15,11 +15,11 @@
 // copied by all of them. A CTA is one warp: the lanes poll the flags of a chunk's
 // bands together, and lane 0 moves the chunk with TMA bulk copies through a
 // six-slot shared-memory ring (global -> shared completes on an mbarrier,
-// shared -> global as a bulk group). A group is (sender o, destination s). When a
-// CTA has stored the last of its chunks of a group, the group joins a release
-// batch: at the CTA's next wait (or its end) it waits for its stores, issues one
-// fence for the whole batch and one release increment of each group's chunk
-// count; the increment that completes a group stores the group signal.
+// shared -> global as a bulk group). A group is (sender o, destination s). At
+// each wait for the producer, and at its end, a CTA waits for its stores, issues
+// one fence, and adds to each group's chunk count the chunks of it stored since
+// the last release (one release increment per group, the groups spread over the
+// lanes); the increment that completes a group stores the group signal.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -33,8 +33,7 @@ constexpr int kRecBatch = 32 * kRecPerLane;  // segment records per batch
 
 struct ConsumerSmem {
   uint64_t full[kChunkSlots];
-  int owned[kMaxGroups];        // this CTA's chunks of each group not yet stored
-  int total[kMaxGroups];        // this CTA's chunks of each group
+  int stored[kMaxGroups];       // chunks of each group stored since the last release
   int rec[kRecBatch][kSegRec];  // a batch of segment records
   int list[kListCap];           // owned chunks of the batch: (record << 20) | chunk index
 };
@@ -64,36 +63,11 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   const int c = blockIdx.x, G = gridDim.x;
   const size_t row_bytes = (size_t)d.D * 2;
 
-  for (int g = lane; g < kMaxGroups; g += 32) sm.owned[g] = 0;
+  for (int g = lane; g < kMaxGroups; g += 32) sm.stored[g] = 0;
   if (lane == 0) {
     for (int i = 0; i < kChunkSlots; ++i) mbar_init(&sm.full[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncwarp();
-  // Pre-pass: how many chunks of each group this CTA copies (8 records per lane
-  // per round, their loads independent).
-  for (int base = 0; base < nseg; base += 32 * 8) {
-    int4 lo[8], hi[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int idx = base + u * 32 + lane;
-      if (idx < nseg) {
-        const int4* r = reinterpret_cast<const int4*>(recs + (size_t)idx * kSegRec);
-        lo[u] = r[0];
-        hi[u] = r[1];
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int idx = base + u * 32 + lane;
-      if (idx < nseg) {
-        const int n = owned_count(hi[u].z, hi[u].w, c, G);
-        if (n) atomicAdd(&sm.owned[lo[u].x * d.W + lo[u].y], n);
-      }
-    }
-  }
-  __syncwarp();
-  for (int g = lane; g < kMaxGroups; g += 32) sm.total[g] = sm.owned[g];
   __syncwarp();
 
   // Copy pipeline, driven by lane 0. Chunk i (in this CTA's order) uses slot i % S
@@ -109,7 +83,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   };
   Pend pend[kChunkSlots] = {};
   int n = 0, stored = 0;
-  unsigned long long finished = 0;  // groups whose chunks (of this CTA) are all stored
+  bool unreleased = false;  // lane 0: chunks stored since the last release
   bool ok = true;
   const long long itimeout = a.p.timeout_ns + 4000000000LL;
 
@@ -122,27 +96,38 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     bulk_store(pend[slot].dst, slots + (size_t)slot * kChunkBytes, pend[slot].bytes);
     bulk_commit();
     ++stored;
-    const int g = pend[slot].group;
-    if (--sm.owned[g] == 0) finished |= 1ull << g;
+    ++sm.stored[pend[slot].group];
+    unreleased = true;
   };
   auto store_landed = [&]() {  // lane 0: store every leading chunk whose load has landed
-    while (stored < n && mbar_try_wait(&sm.full[stored % kChunkSlots], (stored / kChunkSlots) & 1))
+    while (stored < n && mbar_test_wait(&sm.full[stored % kChunkSlots], (stored / kChunkSlots) & 1))
       store_one();
   };
-  // One fence for every group this CTA has finished since the last release, then
-  // one count increment per group; the increment that completes a group signals it.
-  auto release_finished = [&]() {  // lane 0
-    if (finished == 0) return;
-    bulk_wait_all();
-    fence_proxy_async_global();
-    fence_acq_rel_gpu();
-    while (finished) {
-      const int g = __ffsll((long long)finished) - 1;
-      finished &= finished - 1;
-      const uint32_t mine = (uint32_t)sm.total[g];
-      const uint32_t done = atomicAdd(group_done + g, mine) + mine;
-      if (done == (uint32_t)gchunks[g]) st_release_u32(group_sig + g, 1u);
+  // Every lane, at a warp-uniform point: lane 0 waits for its stores and fences
+  // once; then each lane adds the stored chunks of its groups (g = lane, lane + 32)
+  // to their counts with a release increment; the increment that completes a
+  // group stores its signal.
+  auto release_stored = [&]() {
+    if (__shfl_sync(0xffffffffu, unreleased ? 1 : 0, 0) == 0) return;
+    if (lane == 0) {
+      bulk_wait_all();
+      fence_proxy_async_global();
+      fence_acq_rel_gpu();
+      unreleased = false;
     }
+    __syncwarp();
+    for (int g = lane; g < kMaxGroups; g += 32) {
+      const uint32_t mine = (uint32_t)sm.stored[g];
+      if (mine == 0) continue;
+      sm.stored[g] = 0;
+      fence_acq_rel_gpu();
+      const uint32_t done = atomicAdd(group_done + g, mine) + mine;
+      if (done == (uint32_t)gchunks[g]) {
+        fence_acq_rel_gpu();
+        st_release_u32(group_sig + g, 1u);
+      }
+    }
+    __syncwarp();
   };
 
   // Rows and flags of listed chunk `e` (a packed list entry).
@@ -152,7 +137,10 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     r0 = k * d.rpc;
     r1 = min(sm.rec[q][4], r0 + d.rpc);
   };
-  // Acquire reads of the ready flags of one chunk (a subset of them per lane).
+  // Relaxed reads of the ready flags of one chunk (a subset of them per lane), all
+  // in flight together; a caller that found them set issues one acquire fence per
+  // lane (fence.acq_rel after the reads that observed the producer's release
+  // increments) before the copies that read the chunk.
   auto flags_ready = [&](int q, int r0, int r1, int lane_lo, int lane_step) {
     const int b0 = sm.rec[q][2];
     const size_t rb = (size_t)sm.rec[q][0] * d.NBM;
@@ -160,7 +148,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     const uint32_t* f = flags + (rb + bl) * d.nt2;
     const int nflags = (bh - bl + 1) * d.nt2;
     bool ready = true;
-    for (int i = lane_lo; i < nflags; i += lane_step) ready &= ld_acquire_u32(f + i) >= (uint32_t)d.parts;
+    for (int i = lane_lo; i < nflags; i += lane_step) ready &= ld_relaxed_u32(f + i) >= (uint32_t)d.parts;
     return ready;
   };
 
@@ -238,19 +226,19 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
       }
       unsigned long long ready = (unsigned long long)__ballot_sync(0xffffffffu, r0ok) |
                                  ((unsigned long long)__ballot_sync(0xffffffffu, r1ok) << 32);
-      __syncwarp();  // orders lane 0's copies after every lane's acquire
+      fence_acq_rel_gpu();  // each lane: its flag reads become acquires
+      __syncwarp();         // orders lane 0's copies after every lane's acquire
       // The flags were acquired (generic proxy); the bulk loads read Y (async proxy).
       if (lane == 0) fence_proxy_async_global();
       for (int j = 0; j < m && ok; ++j) {
         int q, r0, r1;
         chunk_of(sm.list[s0 + j], q, r0, r1);
         if (!(ready >> j & 1ull)) {
-          // Not produced yet: store everything loaded, release finished groups,
+          // Not produced yet: store everything loaded, release the stored chunks,
           // then wait (bounded, all lanes).
-          if (lane == 0) {
+          if (lane == 0)
             while (stored < n) store_one();
-            release_finished();
-          }
+          release_stored();
           const unsigned long long t0 = globaltimer();
           bool done = false, stop = false;
           while (!done && !stop) {
@@ -289,6 +277,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
           ready = (unsigned long long)__ballot_sync(0xffffffffu, a0ok) |
                   ((unsigned long long)__ballot_sync(0xffffffffu, a1ok) << 32);
           ready |= j == 63 ? ~0ull : ((1ull << (j + 1)) - 1ull);
+          fence_acq_rel_gpu();
           __syncwarp();
           if (lane == 0) fence_proxy_async_global();
         }
@@ -315,12 +304,11 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
     base += take;
   }
   // Drain: store what was loaded (even after an error, so no copy outlives the
-  // CTA's shared memory), release the finished groups, wait for every store.
-  if (lane == 0) {
+  // CTA's shared memory), release the stored chunks, wait for every store.
+  if (lane == 0)
     while (stored < n) store_one();
-    release_finished();
-    bulk_wait_all();
-  }
+  release_stored();
+  if (lane == 0) bulk_wait_all();
 }
 
 }  // namespace
