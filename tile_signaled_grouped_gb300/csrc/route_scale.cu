@@ -11,14 +11,16 @@
 namespace moe {
 namespace {
 
-constexpr int kMaxPerLane = 32;  // E <= 1024
-
 // One warp per token: softmax over E logits (fp32), then k rounds of a warp
 // argmax on (logit descending, expert id ascending). Comparing logits decides
-// the same order as comparing probabilities, without rounding ties.
-__global__ void route_kernel(DevPlan p, const float* __restrict__ logits,
-                             const int32_t* __restrict__ forced, int32_t* __restrict__ ids,
-                             float* __restrict__ w) {
+// the same order as comparing probabilities, without rounding ties. Each lane
+// holds PER logits (E <= 32 * PER); the launcher picks the smallest PER.
+template <int PER>
+__global__ void __launch_bounds__(256) route_kernel(DevPlan p, const float* __restrict__ logits,
+                                                    const int32_t* __restrict__ forced,
+                                                    int32_t* __restrict__ ids,
+                                                    float* __restrict__ w) {
+  constexpr int kMaxPerLane = PER;
   const Dims d = p.d;
   const int lane = threadIdx.x & 31;
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -163,10 +165,24 @@ namespace {
 int g_scale_blocks_per_sm = 0;  // resident scale blocks per SM (set at preload)
 }
 
+template <int PER>
+cudaError_t launch_route_per(const DevPlan& p, const float* logits, const int32_t* forced,
+                             int32_t* ids, float* w, cudaStream_t s) {
+  const int ntok = p.d.W * p.d.T;
+  route_kernel<PER><<<(ntok * 32 + 255) / 256, 256, 0, s>>>(p, logits, forced, ids, w);
+  return cudaGetLastError();
+}
+
 cudaError_t preload_route_scale() {
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, route_kernel);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if ((e = cudaFuncGetAttributes(&fa, route_kernel<1>)) != cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, route_kernel<2>)) != cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, route_kernel<4>)) != cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, route_kernel<8>)) != cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, route_kernel<16>)) != cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, route_kernel<32>)) != cudaSuccess)
+    return e;
   if ((e = cudaFuncGetAttributes(&fa, scale_kernel)) != cudaSuccess) return e;
   int n = 0;
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scale_kernel, 256, 0)) != cudaSuccess)
@@ -177,9 +193,13 @@ cudaError_t preload_route_scale() {
 
 cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* forced,
                          int32_t* ids, float* w, cudaStream_t s) {
-  const int ntok = p.d.W * p.d.T;
-  route_kernel<<<(ntok * 32 + 255) / 256, 256, 0, s>>>(p, logits, forced, ids, w);
-  return cudaGetLastError();
+  const int E = p.d.E;  // at most 1024 (checked when the plan is created)
+  if (E <= 32) return launch_route_per<1>(p, logits, forced, ids, w, s);
+  if (E <= 64) return launch_route_per<2>(p, logits, forced, ids, w, s);
+  if (E <= 128) return launch_route_per<4>(p, logits, forced, ids, w, s);
+  if (E <= 256) return launch_route_per<8>(p, logits, forced, ids, w, s);
+  if (E <= 512) return launch_route_per<16>(p, logits, forced, ids, w, s);
+  return launch_route_per<32>(p, logits, forced, ids, w, s);
 }
 
 cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s) {
