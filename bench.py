@@ -101,12 +101,12 @@ def producer_traffic(wl_name: str, tokens_override: int, pairs: int):
 
     if wl_name != WORKLOAD or tokens_override:
         return None
-    summary, src = (("ffn_pair_a100_like.md", "ffn_pair.cu") if pairs
-                    else ("ffn_producer_a100_like.md", "ffn.cu"))
+    summary, srcs = (("ffn_pair_a100_like.md", ("ffn_pair.cu", "combine_copy.cuh")) if pairs
+                     else ("ffn_producer_a100_like.md", ("ffn.cu",)))
     try:
         text = open(os.path.join(ROOT, "profiles", summary)).read()
         h = hashlib.sha256()
-        for f in (src, "moe_common.cuh"):
+        for f in srcs + ("moe_common.cuh",):
             h.update(open(os.path.join(ROOT, "tile_signaled_grouped_gb300", "csrc", f), "rb").read())
     except OSError:
         return None
@@ -230,6 +230,9 @@ def gpu_arm(args, rank, world, local_rank):
         "config": {"workload": wl.name, "W": W, "experts_per_rank": wl.L, "topk": k,
                    "tokens_per_rank": T, "d_model": D, "d_ff": F, "tb_M": wl.tb_M,
                    "mgb": wl.mgb, "consumer_ctas": args.consumer_ctas,
+                   "schedule": ("fused (copy warp in every producer CTA)" if args.consumer_ctas < 0
+                                else "serial" if args.consumer_ctas == 0
+                                else "overlapped (consumer kernel on its own SMs)"),
                    "producer": "CTA pairs (cta_group::2, M=256)" if args.producer_pairs
                    else "one CTA per tile (M=128)",
                    "producer_ctas": launch[0], "consumer_ctas_launched": launch[1],
@@ -293,7 +296,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     # Consumer CTAs beside the producer: whole-step time for a few partitions.
     sweep = {}
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for cc in [c for c in args.ccta_sweep if c >= 0]:
+    for cc in [c for c in args.ccta_sweep if c >= -1]:
         lay = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, cc,
                             producer_pairs=args.producer_pairs)
         for _ in range(3):
@@ -448,9 +451,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--consumer-ctas", type=int, default=4,
-                    help="consumer CTAs beside the producer; 0 runs the two kernels serially "
-                         "(needed under a profiler, which serialises kernel launches)")
+    ap.add_argument("--consumer-ctas", type=int, default=-1,
+                    help="-1: the copy runs in a warp of every pair-producer CTA (fused); "
+                         "0: producer then consumer, serially; n > 0: n consumer CTAs beside "
+                         "the producer (two kernels, two streams)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -458,10 +462,12 @@ def main():
     ap.add_argument("--producer-pairs", type=int, default=1, choices=[0, 1],
                     help="1: the CTA-pair producer (clusters of two, tcgen05 cta_group::2)")
     ap.add_argument("--ccta-sweep", type=lambda v: [int(x) for x in v.split(",") if x],
-                    default=[0, 2, 4, 8, 16],
+                    default=[-1, 0, 4, 8],
                     help="consumer-CTA counts whose step time is reported (outside the timed "
                          "region); 0 is the serial schedule")
     args = ap.parse_args()
+    if args.consumer_ctas < 0 and not args.producer_pairs:
+        ap.error("--consumer-ctas -1 (fused) needs the pair producer (--producer-pairs 1)")
     if args.warmup < 3:
         args.warmup = 3
 

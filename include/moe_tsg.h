@@ -47,6 +47,9 @@ typedef struct CUstream_st *moe_stream_t;
 /* Largest number of logical ranks one plan can hold. */
 #define MOE_MAX_RANKS 8
 
+/* moe_cfg.consumer_ctas value: the combine copy runs inside the pair producer. */
+#define MOE_CONSUMER_FUSED (-1)
+
 enum moe_error {
   MOE_OK = 0,
   MOE_ERR_ARG = -1,         /* invalid configuration or argument */
@@ -72,7 +75,10 @@ typedef struct moe_cfg {
   int mgb;           /* row bands merged into one middle segment (section 5.2), >= 1 */
   int consumer_ctas; /* consumer CTAs running beside the producer (cCTA of section 5.3).
                         0 = serial: the producer uses every SM, then the consumer runs
-                        on every SM after it, on the producer stream. */
+                        on every SM after it, on the producer stream.
+                        MOE_CONSUMER_FUSED (-1, with producer_pairs = 1): no consumer
+                        kernel; one warp of every producer CTA polls the flags and
+                        copies, on every SM. */
   long long timeout_ns; /* bound on every device-side wait; <= 0 selects 2 s */
   int producer_pairs; /* 0: one producer CTA per 128-row tile (tcgen05.mma, M = 128).
                          1: CTA pairs (clusters of two): each task covers two 128-row
@@ -171,6 +177,14 @@ int moe_scale(moe_plan *plan, const float *topk_w, const void *const *recv, void
  * calls that overlap on the GPU (other streams, other threads) race; serialise them. */
 int moe_plan_build_noalloc(const moe_cfg *cfg, const int32_t *topk_ids, void *plan_out,
                            size_t plan_out_bytes, moe_stream_t stream);
+
+/* Changes the schedule of an existing plan: the consumer partition (consumer_ctas of
+ * moe_cfg; 0 = serial) and the segment merge width (mgb of moe_cfg, section 5.2). Host
+ * only; a new mgb takes effect at the next moe_plan_build, a new consumer_ctas at the
+ * next moe_expert_combine. Same limits as in moe_cfg: MOE_ERR_ARG for values out of
+ * range, MOE_ERR_UNSUPPORTED if a segment of mgb bands would exceed the copy-chunk limit.
+ * The workspaces are unchanged (their sizes do not depend on either value). */
+int moe_set_schedule(moe_plan *plan, int consumer_ctas, int mgb);
 
 /* How moe_expert_combine splits the GPU for this plan (pure host query; the
  * occupancy is read once by moe_plan_create).

@@ -51,17 +51,17 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0, pairs=0):
-    # pairs=0 keeps the one-CTA producer under test here; tests/test_gpu_pairs.py
-    # covers the pair producer.
-    """The whole path through the C ABI. mode: 'overlap' (two streams) or 'serial';
-    pairs: 1 runs the CTA-pair producer."""
+    """The whole path through the C ABI. mode: 'overlap' (two streams), 'serial', or
+    'fused' (the copy inside the pair producer); pairs: 1 runs the CTA-pair producer
+    (0, the default here, keeps the one-CTA producer under test)."""
+    cc = {"overlap": consumer_ctas, "serial": 0, "fused": -1}[mode]
     layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb,
-                          consumer_ctas if mode == "overlap" else 0, timeout_ns, pairs)
+                          cc, timeout_ns, 1 if mode == "fused" else pairs)
     sp = torch.cuda.Stream()
     sc = torch.cuda.Stream(priority=-1)
     torch.cuda.synchronize()
     layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
-                  producer=sp, consumer=sc if mode == "overlap" else None)
+                  producer=sp, consumer=None if mode == "serial" else sc)
     torch.cuda.synchronize()
     return layer
 

@@ -105,3 +105,47 @@ def test_pairs_device_wait_timeout_is_reported_and_recoverable():
     layer.close()
     layer = P.run_gpu(wl, inp, pairs=1)
     assert layer.status() == (0, 0)
+
+
+# ---------------------------------------------------------------- fused variant
+# consumer_ctas = MOE_CONSUMER_FUSED: no consumer kernel; one warp of every pair
+# producer CTA polls the flags and copies.
+
+@pytest.mark.parametrize("mgb", [1, 2])
+def test_fused_tiny_full_parity(mgb):
+    _full_check(get_workload("tiny", mgb=mgb), "fused")
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_fused_small_shapes_full_parity(wl):
+    _full_check(wl, "fused")
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_fused_full_size_sampled(name):
+    wl = get_workload(name)
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="fused")
+    assert layer.status() == (0, 0)
+    assert layer.launch_info()[:2] == (layer.launch_info()[2], 0)  # every SM produces
+    ids, w, plan = P.oracle_plan(wl, inp)
+    P.check_plan(layer, wl, plan, ids, w)
+    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=12,
+                               rng=np.random.default_rng(1))
+    sig = layer.field(capi.MOE_PLAN_GROUP_SIG).view(wl.W, wl.W).cpu()
+    sent = torch.zeros(wl.W, wl.W, dtype=torch.bool)
+    for o in range(wl.W):
+        for dst in plan.band_dst[o]:
+            sent[o, int(dst)] |= int(dst) != o
+    assert torch.equal(sig.bool(), sent), "group signals"
+
+
+def test_fused_device_wait_timeout_is_reported_and_recoverable():
+    wl = get_workload("a100_like")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="fused", timeout_ns=20_000)
+    code, _ = layer.status()
+    assert code == capi.MOE_DEV_TIMEOUT
+    layer.close()
+    layer = P.run_gpu(wl, inp, mode="fused")
+    assert layer.status() == (0, 0)

@@ -2,6 +2,8 @@
 overlapped with compute. Each step's host output must equal the output of a plain
 forward on device inputs, bit for bit, although consecutive steps use different
 inputs and the double-buffered device sets alternate."""
+import dataclasses
+
 import pytest
 import torch
 
@@ -49,3 +51,35 @@ def test_pipelined_steps_equal_plain_forward(name):
     for i, hout in zip(order, houts):
         for got, ref in zip(hout, want[i]):
             assert torch.equal(got, ref), f"step with input set {i}"
+
+
+def test_tuned_schedule_keeps_results_exact():
+    """The adaptive schedule picks one of its candidates; the plan it then builds (new
+    mgb) matches the oracle bit for bit, and the outputs the one-shot forward's."""
+    from tests import parity as P
+    from tile_signaled_grouped_gb300 import capi
+
+    from tests.test_gpu_parity import SMALL
+    wl = SMALL[0]  # W=3, tb_M=64, mgb=3
+    inp = P.inputs_for(wl)
+    torch.cuda.synchronize()
+    layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb,
+                          consumer_ctas=4)
+    cands = ((0, 1), (4, 1), (2, 2), (8, 3))
+    cc, mgb, times = layer.tune(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits,
+                                inp.forced_ids, candidates=cands, steps=2)
+    assert (cc, mgb) in times and set(times) == set(cands)
+    assert layer.launch_info()[1] == cc
+    sp = torch.cuda.Stream()
+    layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                  producer=sp, consumer=torch.cuda.Stream(priority=-1))
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    wl_t = dataclasses.replace(wl, mgb=mgb)
+    ids, w, plan = P.oracle_plan(wl_t, inp)
+    P.check_plan(layer, wl_t, plan, ids, w)
+    P.check_layout_and_outputs(layer, wl_t, inp, plan, ids, w)
+    with pytest.raises(capi.MoeError, match="ARG"):
+        layer.set_schedule(-3, 1)
+    with pytest.raises(capi.MoeError, match="ARG"):
+        layer.set_schedule(4, 0)

@@ -59,6 +59,9 @@ def _parse_enums():
 
 ENUMS = _parse_enums()
 globals().update(ENUMS)
+# Integer #defines of the header (MOE_MAX_RANKS, MOE_CONSUMER_FUSED, ...).
+DEFINES = {n: int(v) for n, v in re.findall(r"#define\s+(MOE_\w+)\s+\(?(-?\d+)\)?", open(HEADER).read())}
+globals().update(DEFINES)
 
 
 def load():
@@ -84,6 +87,7 @@ def load():
         "moe_timings": (ip, [vp, P(ctypes.c_float), ip]),
         "moe_plan_build_noalloc": (ip, [P(moe_cfg), vp, vp, sz, vp]),
         "moe_launch_info": (ip, [vp, P(ip), P(ip), P(ip), P(ip)]),
+        "moe_set_schedule": (ip, [vp, ip, ip]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -189,3 +193,7 @@ def moe_launch_info(plan):
     v = [ctypes.c_int() for _ in range(4)]
     check(lib().moe_launch_info(plan, *[ctypes.byref(x) for x in v]), "moe_launch_info")
     return tuple(x.value for x in v)
+
+
+def moe_set_schedule(plan, consumer_ctas: int, mgb: int):
+    check(lib().moe_set_schedule(plan, consumer_ctas, mgb), "moe_set_schedule")

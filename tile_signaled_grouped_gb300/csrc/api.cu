@@ -31,7 +31,8 @@ struct moe_plan {
   size_t counts[PA_COUNT];
   RankLayout rl;
   int num_sms;
-  int pair_clusters;  // CTA pairs of the pair producer resident at once (0: unknown)
+  int pair_clusters;        // CTA pairs of the pair producer resident at once (0: unknown)
+  int pair_clusters_fused;  // the same for its fused variant
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   cudaEvent_t ev_ready, ev_join;
   cudaEvent_t ev_t0[kTSlots][kTRing], ev_t1[kTSlots][kTRing];
@@ -50,8 +51,9 @@ int dims_from_cfg(const moe_cfg* c, Dims* d) {
   if (c->d_model < 128 || c->d_model % 128 || c->d_ff < 128 || c->d_ff % 128) return MOE_ERR_ARG;
   if (c->d_model > 16384 || c->d_ff > 65536) return MOE_ERR_UNSUPPORTED;  // a row fits one copy chunk
   if (c->tb_M != 64 && c->tb_M != 128 && c->tb_M != 256) return MOE_ERR_ARG;
-  if (c->mgb < 1 || c->consumer_ctas < 0) return MOE_ERR_ARG;
   if (c->producer_pairs != 0 && c->producer_pairs != 1) return MOE_ERR_ARG;
+  if (c->mgb < 1 || c->consumer_ctas < -1) return MOE_ERR_ARG;
+  if (c->consumer_ctas == MOE_CONSUMER_FUSED && c->producer_pairs != 1) return MOE_ERR_ARG;
   Dims x{};
   x.W = c->W;
   x.L = c->L;
@@ -165,10 +167,12 @@ struct LaunchShape {
 // the rest had finished.
 LaunchShape launch_shape(const moe_plan* p, bool serial) {
   LaunchShape ls{};
-  ls.consumer = serial ? p->num_sms : p->cfg.consumer_ctas;
-  ls.producer = serial ? p->num_sms : p->num_sms - p->cfg.consumer_ctas;
+  const bool fused = p->cfg.consumer_ctas == MOE_CONSUMER_FUSED;
+  ls.consumer = serial ? p->num_sms : fused ? 0 : p->cfg.consumer_ctas;
+  ls.producer = serial || fused ? p->num_sms : p->num_sms - p->cfg.consumer_ctas;
   if (p->cfg.producer_pairs) {
-    if (p->pair_clusters > 0) ls.producer = std::min(ls.producer, 2 * p->pair_clusters);
+    const int clusters = fused ? p->pair_clusters_fused : p->pair_clusters;
+    if (clusters > 0) ls.producer = std::min(ls.producer, 2 * clusters);
     ls.producer = std::max(2, ls.producer & ~1);
   }
   return ls;
@@ -285,7 +289,8 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
   std::memcpy(p->counts, cnt, sizeof(cnt));
   p->rl = rl;
   p->num_sms = prop.multiProcessorCount;
-  p->pair_clusters = producer_pair_max_clusters();
+  p->pair_clusters = producer_pair_max_clusters(false);
+  p->pair_clusters_fused = producer_pair_max_clusters(true);
   p->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   bool ok = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) == cudaSuccess;
@@ -358,7 +363,8 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
       return MOE_ERR_ARG;
   cudaStream_t sp = reinterpret_cast<cudaStream_t>(producer);
   cudaStream_t sc = reinterpret_cast<cudaStream_t>(consumer);
-  const bool serial = p->cfg.consumer_ctas == 0 || sp == sc;
+  const bool fused = p->cfg.consumer_ctas == MOE_CONSUMER_FUSED;
+  const bool serial = !fused && (p->cfg.consumer_ctas == 0 || sp == sc);
   const bool pairs = p->cfg.producer_pairs != 0;
   const LaunchShape ls = launch_shape(p, serial);
   const int cgrid = ls.consumer, pgrid = ls.producer;
@@ -379,6 +385,7 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
       return MOE_ERR_ARG;
     pa.h[r] = H;
     pa.y[r] = Y;
+    pa.recv[r] = static_cast<__nv_bfloat16*>(recv[r]);
   }
   // GEMM2 tasks of a unit start `lag` units after its GEMM1 tasks: about two
   // tasks per CTA (or CTA pair) in flight separate them. A pair unit holds about
@@ -399,9 +406,13 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
   const size_t z0 = p->offsets[PA_QUEUE];
   const size_t z1 = p->offsets[PA_GROUP_SIG] + p->counts[PA_GROUP_SIG] * 4;
   CUDA_TRY(cudaMemsetAsync(p->plan_ws + z0, 0, z1 - z0, sp));
-  if (serial) {
+  if (fused) {
     tstart(p, kTProducer, sp);
-    CUDA_TRY(pairs ? launch_producer_pair(pa, pgrid, sp) : launch_producer(pa, pgrid, sp));
+    CUDA_TRY(launch_producer_pair(pa, pgrid, true, sp));
+    tstop(p, kTProducer, sp);
+  } else if (serial) {
+    tstart(p, kTProducer, sp);
+    CUDA_TRY(pairs ? launch_producer_pair(pa, pgrid, false, sp) : launch_producer(pa, pgrid, sp));
     tstop(p, kTProducer, sp);
     tstart(p, kTConsumer, sp);
     CUDA_TRY(launch_consumer(ca, cgrid, sp));
@@ -414,7 +425,7 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
     tstop(p, kTConsumer, sc);
     CUDA_TRY(cudaEventRecord(p->ev_join, sc));
     tstart(p, kTProducer, sp);
-    CUDA_TRY(pairs ? launch_producer_pair(pa, pgrid, sp) : launch_producer(pa, pgrid, sp));
+    CUDA_TRY(pairs ? launch_producer_pair(pa, pgrid, false, sp) : launch_producer(pa, pgrid, sp));
     tstop(p, kTProducer, sp);
     CUDA_TRY(cudaStreamWaitEvent(sp, p->ev_join, 0));
   }
@@ -439,6 +450,20 @@ int moe_scale(moe_plan* p, const float* topk_w, const void* const* recv, void* c
   tstart(p, kTScale, s);
   CUDA_TRY(launch_scale(a, p->num_sms, s));
   tstop(p, kTScale, s);
+  return MOE_OK;
+}
+
+int moe_set_schedule(moe_plan* p, int consumer_ctas, int mgb) {
+  if (p == nullptr) return MOE_ERR_ARG;
+  moe_cfg c = p->cfg;
+  c.consumer_ctas = consumer_ctas;
+  c.mgb = mgb;
+  Dims d;
+  const int rc = dims_from_cfg(&c, &d);
+  if (rc != MOE_OK) return rc;
+  if (c.consumer_ctas >= p->num_sms) c.consumer_ctas = p->num_sms / 2;
+  p->cfg = c;
+  p->d = d;
   return MOE_OK;
 }
 

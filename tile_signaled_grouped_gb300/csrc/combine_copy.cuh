@@ -1,0 +1,300 @@
+// Combine copy: the body of the flag-polling consumer, shared by the standalone
+// consumer kernel (its own SMs, beside or after the producer) and the copy warp of
+// the fused pair producer. One warp runs it; see consumer.cu for the method.
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kMaxGroups = MOE_MAX_RANKS * MOE_MAX_RANKS;
+constexpr int kListCap = kMaxSegChunks;  // owned chunks listed per batch of records
+
+// Shared memory of one copying warp: SLOTS chunk slots live elsewhere.
+template <int SLOTS, int REC_PER_LANE>
+struct CopySmem {
+  uint64_t full[SLOTS];
+  int stored[kMaxGroups];                   // chunks of each group stored since the last release
+  int rec[32 * REC_PER_LANE][kSegRec];      // a batch of segment records
+  int list[kListCap];                       // owned chunks of the batch: (record << 20) | chunk index
+};
+
+// Chunks i in [cb, cb + n) with i % G == c.
+__device__ __forceinline__ int owned_count(int cb, int n, int c, int G) {
+  const int i0 = cb + ((c - cb) % G + G) % G;
+  return i0 >= cb + n ? 0 : (cb + n - 1 - i0) / G + 1;
+}
+
+// Copies every chunk i (of all segments, in the producer's tile order) with
+// i % G == c: waits for its ready flags, moves it Y -> receive buffer through
+// SLOTS shared-memory slots of kChunkBytes (at most INFLIGHT loads outstanding),
+// and releases the stored chunks per group at each wait and at the end. Called by
+// all 32 lanes of one warp.
+template <int SLOTS, int INFLIGHT, int REC_PER_LANE>
+__device__ __forceinline__ void combine_copy(const DevPlan& p, const __nv_bfloat16* const* y,
+                                             __nv_bfloat16* const* recv, uint8_t* slots,
+                                             CopySmem<SLOTS, REC_PER_LANE>& sm, int c, int G) {
+  static_assert(INFLIGHT >= 1 && INFLIGHT <= SLOTS, "copy ring");
+  constexpr int kChunkSlots = SLOTS;
+  constexpr int kLoadsInFlight = INFLIGHT;
+  constexpr int kRecPerLane = REC_PER_LANE;
+  const Dims d = p.d;
+  uint32_t* status = reinterpret_cast<uint32_t*>(p.a[PA_STATUS]);
+  const uint32_t* flags = reinterpret_cast<const uint32_t*>(p.a[PA_FLAGS]);
+  uint32_t* group_done = reinterpret_cast<uint32_t*>(p.a[PA_GROUP_DONE]);
+  uint32_t* group_sig = reinterpret_cast<uint32_t*>(p.a[PA_GROUP_SIG]);
+  const int32_t* recs = p.a[PA_SEG_REC];
+  const int32_t* gchunks = p.a[PA_GROUP_NCHUNK];
+  const int nseg = p.a[PA_TOTALS][1];
+  const int lane = threadIdx.x & 31;
+  const size_t row_bytes = (size_t)d.D * 2;
+
+  for (int g = lane; g < kMaxGroups; g += 32) sm.stored[g] = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kChunkSlots; ++i) mbar_init(&sm.full[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // Copy pipeline, driven by lane 0. Chunk i (in this CTA's order) uses slot i % S
+  // and completes phase (i / S) & 1 of that slot's barrier. A chunk is stored as
+  // soon as its load has landed; at most kLoadsInFlight loads are outstanding, so
+  // when a slot is refilled at least S - kLoadsInFlight newer stores follow the
+  // store that last used it, and waiting until only that many may still be reading
+  // frees the slot without waiting for recent stores.
+  struct Pend {
+    uint8_t* dst;
+    uint32_t bytes;
+    int group;
+  };
+  Pend pend[kChunkSlots] = {};
+  int n = 0, stored = 0;
+  bool unreleased = false;  // lane 0: chunks stored since the last release
+  bool ok = true;
+  const long long itimeout = p.timeout_ns + 4000000000LL;
+
+  auto store_one = [&]() {  // lane 0: store chunk `stored` (bounded wait for its load)
+    const int slot = stored % kChunkSlots;
+    volatile int never = 0;
+    if (!mbar_wait_bounded(&sm.full[slot], (stored / kChunkSlots) & 1, &never, itimeout, status,
+                           0x60000000u))
+      ok = false;
+    bulk_store(pend[slot].dst, slots + (size_t)slot * kChunkBytes, pend[slot].bytes);
+    bulk_commit();
+    ++stored;
+    ++sm.stored[pend[slot].group];
+    unreleased = true;
+  };
+  auto store_landed = [&]() {  // lane 0: store every leading chunk whose load has landed
+    while (stored < n && mbar_test_wait(&sm.full[stored % kChunkSlots], (stored / kChunkSlots) & 1))
+      store_one();
+  };
+  // Every lane, at a warp-uniform point: lane 0 waits for its stores and fences
+  // once; then each lane adds the stored chunks of its groups (g = lane, lane + 32)
+  // to their counts with a release increment; the increment that completes a
+  // group stores its signal.
+  auto release_stored = [&]() {
+    if (__shfl_sync(0xffffffffu, unreleased ? 1 : 0, 0) == 0) return;
+    if (lane == 0) {
+      bulk_wait_all();
+      fence_proxy_async_global();
+      fence_acq_rel_gpu();
+      unreleased = false;
+    }
+    __syncwarp();
+    for (int g = lane; g < kMaxGroups; g += 32) {
+      const uint32_t mine = (uint32_t)sm.stored[g];
+      if (mine == 0) continue;
+      sm.stored[g] = 0;
+      fence_acq_rel_gpu();
+      const uint32_t done = atomicAdd(group_done + g, mine) + mine;
+      if (done == (uint32_t)gchunks[g]) {
+        fence_acq_rel_gpu();
+        st_release_u32(group_sig + g, 1u);
+      }
+    }
+    __syncwarp();
+  };
+
+  // Rows and flags of listed chunk `e` (a packed list entry).
+  auto chunk_of = [&](int e, int& q, int& r0, int& r1) {
+    q = e >> 20;
+    const int k = e & 0xFFFFF;
+    r0 = k * d.rpc;
+    r1 = min(sm.rec[q][4], r0 + d.rpc);
+  };
+  // Relaxed reads of the ready flags of one chunk (a subset of them per lane), all
+  // in flight together; a caller that found them set issues one acquire fence per
+  // lane (fence.acq_rel after the reads that observed the producer's release
+  // increments) before the copies that read the chunk.
+  auto flags_ready = [&](int q, int r0, int r1, int lane_lo, int lane_step) {
+    const int b0 = sm.rec[q][2];
+    const size_t rb = (size_t)sm.rec[q][0] * d.NBM;
+    const int bl = b0 + r0 / d.tb, bh = b0 + (r1 - 1) / d.tb;
+    const uint32_t* f = flags + (rb + bl) * d.nt2;
+    const int nflags = (bh - bl + 1) * d.nt2;
+    bool ready = true;
+    for (int i = lane_lo; i < nflags; i += lane_step) ready &= ld_relaxed_u32(f + i) >= (uint32_t)d.parts;
+    return ready;
+  };
+
+  // Records are taken in batches of up to 32 * REC_PER_LANE (loads
+  // independent). Each batch lists this CTA's chunks of as many of its records as
+  // fit in kListCap entries, in order; the flags of 64 listed chunks are checked
+  // per round trip (2 per lane).
+  int base = 0;
+  while (base < nseg && ok) {
+    int cnt[kRecPerLane];
+    int lsum = 0;
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kRecPerLane; ++u) {
+      const int ri = lane * kRecPerLane + u;  // record of the batch, in order
+      const int idx = base + ri;
+      cnt[u] = 0;
+      if (idx < nseg) {
+        const int4* r = reinterpret_cast<const int4*>(recs + (size_t)idx * kSegRec);
+        const int4 lo = r[0], hi = r[1];
+        sm.rec[ri][0] = lo.x; sm.rec[ri][1] = lo.y; sm.rec[ri][2] = lo.z; sm.rec[ri][3] = lo.w;
+        sm.rec[ri][4] = hi.x; sm.rec[ri][5] = hi.y; sm.rec[ri][6] = hi.z; sm.rec[ri][7] = hi.w;
+        cnt[u] = owned_count(hi.z, hi.w, c, G);
+      }
+      lsum += cnt[u];
+    }
+    int incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    // Records that fit: a prefix of the batch (the first record always fits,
+    // because a segment has at most kListCap chunks).
+    int pos = incl - lsum, fit = 0;
+#pragma unroll
+    for (int u = 0; u < kRecPerLane; ++u) {
+      const int idx = base + lane * kRecPerLane + u;
+      if (idx < nseg && pos + cnt[u] <= kListCap) {
+        const int ri = lane * kRecPerLane + u;
+        int k = ((c - sm.rec[ri][6]) % G + G) % G;
+        for (int j = 0; j < cnt[u]; ++j, k += G) sm.list[pos + j] = (ri << 20) | k;
+        pos += cnt[u];
+        ++fit;
+      } else {
+        pos = kListCap + 1;  // later records of the batch wait for the next batch
+      }
+    }
+    int take = fit;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) take += __shfl_xor_sync(0xffffffffu, take, o);
+    take = max(1, take);
+    int nlist = 0;
+    {  // entries written by the fitting records
+      const int last = take - 1;  // last fitting record of the batch
+      const int ll = last / kRecPerLane;
+      int e = incl - lsum;
+      for (int u = 0; u <= last - ll * kRecPerLane; ++u) e += cnt[u];
+      nlist = __shfl_sync(0xffffffffu, e, ll);
+    }
+    __syncwarp();
+
+    for (int s0 = 0; s0 < nlist && ok; s0 += 64) {
+      const int m = min(64, nlist - s0);
+      bool r0ok = true, r1ok = true;
+      if (lane < m) {
+        int q, a0, a1;
+        chunk_of(sm.list[s0 + lane], q, a0, a1);
+        r0ok = flags_ready(q, a0, a1, 0, 1);
+      }
+      if (lane + 32 < m) {
+        int q, a0, a1;
+        chunk_of(sm.list[s0 + 32 + lane], q, a0, a1);
+        r1ok = flags_ready(q, a0, a1, 0, 1);
+      }
+      unsigned long long ready = (unsigned long long)__ballot_sync(0xffffffffu, r0ok) |
+                                 ((unsigned long long)__ballot_sync(0xffffffffu, r1ok) << 32);
+      fence_acq_rel_gpu();  // each lane: its flag reads become acquires
+      __syncwarp();         // orders lane 0's copies after every lane's acquire
+      // The flags were acquired (generic proxy); the bulk loads read Y (async proxy).
+      if (lane == 0) fence_proxy_async_global();
+      for (int j = 0; j < m && ok; ++j) {
+        int q, r0, r1;
+        chunk_of(sm.list[s0 + j], q, r0, r1);
+        if (!(ready >> j & 1ull)) {
+          // Not produced yet: store everything loaded, release the stored chunks,
+          // then wait (bounded, all lanes).
+          if (lane == 0)
+            while (stored < n) store_one();
+          release_stored();
+          const unsigned long long t0 = globaltimer();
+          bool done = false, stop = false;
+          while (!done && !stop) {
+            done = __all_sync(0xffffffffu, flags_ready(q, r0, r1, lane, 32));
+            if (!done) {
+              __nanosleep(64);
+              if (lane == 0) {
+                if (ld_relaxed_u32(status) != 0) {
+                  stop = true;
+                } else if ((long long)(globaltimer() - t0) > p.timeout_ns) {
+                  const int bl = sm.rec[q][2] + r0 / d.tb;
+                  report_error(status, MOE_DEV_TIMEOUT,
+                               0x50000000u | (uint32_t)((size_t)sm.rec[q][0] * d.NBM + bl));
+                  stop = true;
+                }
+              }
+              stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+            }
+          }
+          if (stop) {
+            ok = false;
+            break;
+          }
+          // Chunks after this one may have become ready meanwhile.
+          bool a0ok = true, a1ok = true;
+          if (lane > j && lane < m) {
+            int q2, b0, b1;
+            chunk_of(sm.list[s0 + lane], q2, b0, b1);
+            a0ok = flags_ready(q2, b0, b1, 0, 1);
+          }
+          if (lane + 32 > j && lane + 32 < m) {
+            int q2, b0, b1;
+            chunk_of(sm.list[s0 + 32 + lane], q2, b0, b1);
+            a1ok = flags_ready(q2, b0, b1, 0, 1);
+          }
+          ready = (unsigned long long)__ballot_sync(0xffffffffu, a0ok) |
+                  ((unsigned long long)__ballot_sync(0xffffffffu, a1ok) << 32);
+          ready |= j == 63 ? ~0ull : ((1ull << (j + 1)) - 1ull);
+          fence_acq_rel_gpu();
+          __syncwarp();
+          if (lane == 0) fence_proxy_async_global();
+        }
+        if (lane == 0) {
+          store_landed();
+          while (n - stored >= kLoadsInFlight) store_one();
+          if (n >= kChunkSlots) bulk_wait_read<kChunkSlots - kLoadsInFlight>();
+          const int o = sm.rec[q][0], dst = sm.rec[q][1], b0 = sm.rec[q][2];
+          const int slot = n % kChunkSlots;
+          const uint32_t bytes = (uint32_t)((size_t)(r1 - r0) * row_bytes);
+          const uint8_t* src =
+              reinterpret_cast<const uint8_t*>(y[o]) + ((size_t)b0 * d.tb + r0) * row_bytes;
+          pend[slot].dst =
+              reinterpret_cast<uint8_t*>(recv[dst]) + ((size_t)sm.rec[q][5] + r0) * row_bytes;
+          pend[slot].bytes = bytes;
+          pend[slot].group = o * d.W + dst;
+          mbar_arrive_expect_tx(&sm.full[slot], bytes);
+          bulk_load(slots + (size_t)slot * kChunkBytes, src, bytes, &sm.full[slot]);
+          ++n;
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      }
+    }
+    base += take;
+  }
+  // Drain: store what was loaded (even after an error, so no copy outlives the
+  // CTA's shared memory), release the stored chunks, wait for every store.
+  if (lane == 0)
+    while (stored < n) store_one();
+  release_stored();
+  if (lane == 0) bulk_wait_all();
+}
+
+}  // namespace moe

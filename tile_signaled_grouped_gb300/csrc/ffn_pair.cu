@@ -25,6 +25,10 @@
 // The accumulator is freed for reuse when both CTAs' epilogues have arrived on
 // the leader's tempty barrier.
 //
+// Fused variant (consumer_ctas = MOE_CONSUMER_FUSED): every CTA also runs the
+// combine copy in one more warp (the standalone consumer's body with one chunk
+// slot), so no SM is set aside for the consumer; the pipeline keeps six stages.
+//
 // Waits. A GEMM2 task waits (bounded by timeout_ns) until its tile's GEMM1 tiles
 // are counted; on expiry it records MOE_DEV_TIMEOUT and still completes the task
 // (its result is void), so the two CTAs never disagree on the task sequence; the
@@ -32,17 +36,17 @@
 // depends only on the pair's own progress and is bounded by timeout_ns + 4 s.
 // The CTAs meet in a cluster barrier only at the start (barriers and TMEM ready
 // in both) and at the end (every MMA drained, every copy landed), then free TMEM.
-#include "moe_common.cuh"
+#include "combine_copy.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kPStages = 7;
+constexpr int kPMaxStages = 7;  // pipeline depth (the fused variant uses one stage less)
 // Warp roles: warp 0 TMA, warp 1 MMA (rank 0 only), warps 2-9 epilogue, warp 10
 // scheduler (lane 0 of each single-thread role works; its other lanes idle).
 constexpr int kEpiWarp0 = 2, kEpiWarps = 8;
 constexpr int kSchedWarp = kEpiWarp0 + kEpiWarps;
-constexpr int kPairThreads = 32 * (kSchedWarp + 1);
+constexpr int kCopyWarp = kSchedWarp + 1;  // fused variant: the combine copy
 static_assert(kEpiWarps % 4 == 0, "each epilogue group covers all four TMEM lane quarters");
 constexpr int kPRing = 2;  // posted tasks in flight inside one CTA (more widens the L2 working set)
 constexpr int kHRing = 4;  // tickets in flight from rank 0 to rank 1
@@ -65,7 +69,7 @@ struct PTask {
 };
 
 struct PSmem {
-  uint64_t full[kPStages], empty[kPStages];
+  uint64_t full[kPMaxStages], empty[kPMaxStages];
   uint64_t tfull[2], tempty[2];
   uint64_t qfull[kPRing], qempty[kPRing];
   uint64_t hfull[kHRing], hempty[kHRing];  // ticket hand-off: hfull in rank 1, hempty in rank 0
@@ -80,9 +84,19 @@ struct PSmem {
   int unit_begin[kPUnitCache + 1];
 };
 
-constexpr size_t kPSmemBytes =
-    1024 /*alignment slack*/ + (size_t)kPStages * (kPABytes + kPBBytes) + sizeof(PSmem);
-static_assert(kPSmemBytes <= 227 * 1024, "pair producer shared memory");
+// The fused variant also runs the combine copy in warp kCopyWarp: one chunk slot
+// and the copy state, paid for with one pipeline stage.
+using PairCopySmem = CopySmem<1, 2>;
+template <bool FUSED>
+struct PairCfg {
+  static constexpr int kStages = FUSED ? kPMaxStages - 1 : kPMaxStages;
+  static constexpr int kThreads = 32 * (kSchedWarp + 1 + (FUSED ? 1 : 0));
+  static constexpr size_t kStageBytes = (size_t)kStages * (kPABytes + kPBBytes);
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStageBytes + sizeof(PSmem) +
+                                  (FUSED ? (size_t)kChunkBytes + sizeof(PairCopySmem) + 16 : 0);
+};
+static_assert(PairCfg<false>::kSmem <= 227 * 1024, "pair producer shared memory");
+static_assert(PairCfg<true>::kSmem <= 227 * 1024, "fused pair producer shared memory");
 
 // --- cluster and cta_group::2 forms ------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -235,8 +249,10 @@ __device__ PTask decode_ticket(const PSmem& sm, const ProducerArgs& a, long long
   return tk;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+template <bool FUSED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThreads, 1)
     ffn_pair_kernel(const __grid_constant__ ProducerArgs a) {
+  constexpr int kPStages = PairCfg<FUSED>::kStages;
   extern __shared__ uint8_t smem_raw[];
   const Dims d = a.p.d;
   const uint32_t raw = smem_u32(smem_raw);
@@ -245,6 +261,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   uint8_t* a_tiles = stage_base;                                // kPStages x 16 KB
   uint8_t* b_tiles = stage_base + (size_t)kPStages * kPABytes;  // kPStages x 16 KB
   PSmem& sm = *reinterpret_cast<PSmem*>(stage_base + (size_t)kPStages * (kPABytes + kPBBytes));
+  // Fused variant: the copy slot (16-byte aligned) and the copy state follow.
+  uint8_t* copy_slot = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(&sm + 1) + 15) & ~static_cast<uintptr_t>(15));
+  PairCopySmem& csm = *reinterpret_cast<PairCopySmem*>(copy_slot + kChunkBytes);
 
   uint32_t* status = reinterpret_cast<uint32_t*>(a.p.a[PA_STATUS]);
   uint32_t* queue = reinterpret_cast<uint32_t*>(a.p.a[PA_QUEUE]);
@@ -292,7 +312,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
 
-  if (warp == kSchedWarp && lane == 0) {
+  if (FUSED && warp == kCopyWarp) {
+    // ------------------------------------------------------------ combine copy
+    // Every CTA of the grid copies its share of the finished segments (chunk i
+    // when i % grid == CTA index), polling the ready flags, exactly as the
+    // standalone consumer does on its own SMs.
+    combine_copy<1, 1, 2>(a.p, a.y, a.recv, copy_slot, csm, blockIdx.x, gridDim.x);
+  } else if (warp == kSchedWarp && lane == 0) {
     // ------------------------------------------------------------ scheduler
     // Takes every ticket (rank 0 from the counter, handing it to rank 1), decodes
     // it, makes sure a GEMM2 task's h rows are complete, and posts the task to the
@@ -566,28 +592,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 
 cudaError_t preload_producer_pair() {
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, ffn_pair_kernel);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(ffn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kPSmemBytes);
+  cudaError_t e;
+  if ((e = cudaFuncGetAttributes(&fa, ffn_pair_kernel<false>)) != cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, ffn_pair_kernel<true>)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(ffn_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)PairCfg<false>::kSmem)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(ffn_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)PairCfg<true>::kSmem);
 }
 
-int producer_pair_max_clusters() {
+template <bool FUSED>
+int max_clusters() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.blockDim = dim3(PairCfg<FUSED>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<FUSED>::kSmem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ffn_pair_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, ffn_pair_kernel<FUSED>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-cudaError_t launch_producer_pair(const ProducerArgs& a, int grid, cudaStream_t s) {
+int producer_pair_max_clusters(bool fused) {
+  return fused ? max_clusters<true>() : max_clusters<false>();
+}
+
+cudaError_t launch_producer_pair(const ProducerArgs& a, int grid, bool fused, cudaStream_t s) {
   grid = grid < 2 ? 2 : grid & ~1;
-  ffn_pair_kernel<<<grid, kPairThreads, kPSmemBytes, s>>>(a);
+  if (fused)
+    ffn_pair_kernel<true><<<grid, PairCfg<true>::kThreads, PairCfg<true>::kSmem, s>>>(a);
+  else
+    ffn_pair_kernel<false><<<grid, PairCfg<false>::kThreads, PairCfg<false>::kSmem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -114,6 +114,7 @@ struct ProducerArgs {
   CUtensorMap tm_wd[MOE_MAX_RANKS];
   __nv_bfloat16* h[MOE_MAX_RANKS];
   __nv_bfloat16* y[MOE_MAX_RANKS];
+  __nv_bfloat16* recv[MOE_MAX_RANKS];  // receive buffers (the fused pair producer copies into them)
   DevPlan p;
   int lag;  // scheduling units between a unit's GEMM1 tiles and its GEMM2 tiles
 };
@@ -121,8 +122,10 @@ cudaError_t launch_producer(const ProducerArgs& a, int grid, cudaStream_t s);
 // CTA-pair producer (clusters of two, tcgen05 cta_group::2); grid is rounded down
 // to an even count. Its tm_wd maps use boxes of N2/2 rows.
 cudaError_t preload_producer_pair();
-int producer_pair_max_clusters();  // clusters of two resident at once on an idle GPU (0: unknown)
-cudaError_t launch_producer_pair(const ProducerArgs& a, int grid, cudaStream_t s);
+// Clusters of two resident at once on an idle GPU (0: unknown).
+int producer_pair_max_clusters(bool fused);
+// fused: the variant whose every CTA also runs the combine copy in one warp.
+cudaError_t launch_producer_pair(const ProducerArgs& a, int grid, bool fused, cudaStream_t s);
 
 struct ConsumerArgs {
   const __nv_bfloat16* y[MOE_MAX_RANKS];

@@ -20,8 +20,11 @@ def _stream_handle(s) -> int:
 class ExpertCombine:
     """One MoE layer split over W logical ranks on the current CUDA device."""
 
-    def __init__(self, W, L, topk, T, d_model, d_ff, tb_M, mgb=1, consumer_ctas=8,
-                 timeout_ns=0, producer_pairs=1, device=None):
+    def __init__(self, W, L, topk, T, d_model, d_ff, tb_M, mgb=1,
+                 consumer_ctas=capi.MOE_CONSUMER_FUSED, timeout_ns=0, producer_pairs=1,
+                 device=None):
+        """consumer_ctas: MOE_CONSUMER_FUSED (-1, the copy runs in a warp of every pair
+        producer CTA), 0 (serial), or the consumer CTAs beside the producer."""
         self.device = torch.device(device or "cuda")
         self.cfg = capi.moe_cfg(W, L, topk, T, d_model, d_ff, tb_M, mgb, consumer_ctas,
                                 timeout_ns, producer_pairs)
@@ -111,6 +114,44 @@ class ExpertCombine:
         off, cnt = capi.moe_field(self.cfg, field)
         cols = self.F if field == capi.MOE_RANK_H else self.D
         return self.rank_ws[rank][off:off + 2 * cnt].view(torch.bfloat16).view(-1, cols)
+
+    def set_schedule(self, consumer_ctas: int, mgb: int):
+        """Consumer partition (0 = serial) and segment merge width; the next plan build
+        and combine use them."""
+        capi.moe_set_schedule(self.plan, consumer_ctas, mgb)
+        self.cfg.consumer_ctas, self.cfg.mgb = consumer_ctas, mgb
+
+    def tune(self, x, w_gate, w_up, w_down, logits, forced_ids=None, producer=None,
+             consumer=None, candidates=((-1, 1), (0, 1), (4, 1), (8, 1), (4, 2)), steps=6):
+        """Adaptive schedule: times whole steps on these inputs for each (consumer_ctas,
+        mgb) candidate and keeps the fastest. Returns (consumer_ctas, mgb, {candidate:
+        ms per step}). Candidates the shape does not support are skipped."""
+        sp = producer if producer is not None else torch.cuda.Stream(device=self.device)
+        sc = consumer if consumer is not None else torch.cuda.Stream(device=self.device,
+                                                                     priority=-1)
+        keep = (self.cfg.consumer_ctas, self.cfg.mgb)
+        times = {}
+        for cc, mgb in candidates:
+            try:
+                self.set_schedule(cc, mgb)
+            except capi.MoeError:
+                continue
+            run = lambda: self.forward(x, w_gate, w_up, w_down, logits, forced_ids, sp, sc)
+            run()
+            run()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(sp)
+            for _ in range(steps):
+                run()
+            e1.record(sp)
+            e1.synchronize()
+            if self.status() != (0, 0):
+                raise capi.MoeError(f"device status {self.status()} while tuning {cc, mgb}")
+            times[(cc, mgb)] = e0.elapsed_time(e1) / steps
+        best = min(times, key=times.get) if times else keep
+        self.set_schedule(*best)
+        return best[0], best[1], times
 
     def launch_info(self):
         """(producer_ctas, consumer_ctas, num_sms, pair_clusters) of the overlapped schedule."""
