@@ -312,6 +312,20 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         sweep[str(cc)] = ev0.elapsed_time(ev1) / (iters * 4)
         lay.close()
         del lay
+    # The same step captured once into a CUDA graph and replayed (one host launch per step).
+    layer.set_timing(False)
+    graph = layer.capture(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                          producer=sp, consumer=sc)
+    with torch.cuda.stream(sp):
+        for _ in range(3):
+            graph.replay()
+        ev0.record(sp)
+        for _ in range(iters * 4):
+            graph.replay()
+        ev1.record(sp)
+    torch.cuda.synchronize()
+    graph_ms = ev0.elapsed_time(ev1) / (iters * 4)
+    del graph
     rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
     recv_rows = layer.field(capi.MOE_PLAN_RECV_ROWS).cpu().tolist()
     rows = sum(rank_rows)
@@ -325,6 +339,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         "overlapped_ms": over,
         "serial_ms": ser,
         "step_ms_by_consumer_ctas": sweep,
+        "step_ms_graph_replay": graph_ms,
         "producer_alone_tflops": flops / (ser["producer"] * 1e-3) / 1e12,
         "producer_alone_frac_burst": flops / (ser["producer"] * 1e-3) / 1e12 / bf16,
         "producer_overlapped_tflops": flops / (over["producer"] * 1e-3) / 1e12,

@@ -98,6 +98,22 @@ class ExpertCombine:
         self.expert_combine(w_gate, w_up, w_down, producer, consumer)
         return self.scale(stream=producer, out=out)
 
+    def capture(self, x, w_gate, w_up, w_down, logits, forced_ids=None, producer=None,
+                consumer=None, out=None):
+        """Records one step (route, plan, combine, scale) into a CUDA graph over these
+        tensors. Replaying it (graph.replay()) runs the step on whatever the tensors hold
+        then, with one launch from the host. Every call the step makes is asynchronous
+        and allocates nothing, so the whole path is capturable; the event fork and join
+        between the producer and consumer streams become graph edges."""
+        sp = producer if producer is not None else torch.cuda.Stream(device=self.device)
+        sc = consumer if consumer is not None else torch.cuda.Stream(device=self.device,
+                                                                     priority=-1)
+        torch.cuda.synchronize(self.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=sp):
+            self.forward(x, w_gate, w_up, w_down, logits, forced_ids, sp, sc, out=out)
+        return graph
+
     # ------------------------------------------------------------- inspection
     def status(self, stream=None):
         return capi.moe_status(self.plan, _stream_handle(stream))
