@@ -72,9 +72,10 @@ FULL = ["a100_like", "qwen3_235b_like", "deepseek_v3_like", "stress_skew"]
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled(name):
-    """The five workload shapes at full size, in the launch configuration the bench
-    times (producer and consumer overlapped on two streams): every plan array
-    bit-exact, sampled rows and tokens against the oracle, all copies exact."""
+    """The workload shapes at full size with the one-CTA producer and the consumer
+    kernel overlapped on two streams: every plan array bit-exact, sampled rows and
+    tokens against the oracle, all copies exact. (The schedule the bench times, the
+    fused pair producer, is covered in test_gpu_pairs.py.)"""
     wl = get_workload(name)
     inp = P.inputs_for(wl)
     layer = P.run_gpu(wl, inp, mode="overlap", consumer_ctas=16)
@@ -147,3 +148,27 @@ def test_host_argument_errors():
     with pytest.raises(capi.MoeError, match="ARG"):
         capi.moe_plan_build(plan, 0, [0] * wl.W, 0)
     capi.moe_plan_destroy(plan)
+
+
+# One shape per logits-per-lane instantiation of the route kernel (E <= 32, 64, 128,
+# 256, 512, 1024): routing ids bit-exact, weights to fp32 rounding, and the whole plan
+# bit-exact (the plan kernels hold up to 256 experts per rank).
+ROUTE_SHAPES = [
+    Workload("E16", W=4, L=4, topk=3, T=40, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("E48", W=4, L=12, topk=4, T=40, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("E96", W=8, L=12, topk=6, T=24, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("E200", W=8, L=25, topk=8, T=24, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("E384", W=8, L=48, topk=8, T=16, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("E1024", W=8, L=128, topk=8, T=16, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+]
+
+
+@pytest.mark.parametrize("wl", ROUTE_SHAPES, ids=lambda w: w.name)
+def test_route_and_plan_for_every_expert_count(wl):
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="serial")
+    assert layer.status() == (0, 0)
+    ids, w, plan = P.oracle_plan(wl, inp)
+    P.check_plan(layer, wl, plan, ids, w)
+    P.check_order(layer, wl, plan)
+    layer.close()
