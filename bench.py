@@ -150,21 +150,31 @@ def gpu_arm(args, rank, world, local_rank):
     W, T, D, F, k = wl.W, wl.T, wl.d_model, wl.d_ff, wl.topk
     inp = make_inputs(wl, device="cuda")
     torch.cuda.synchronize()  # inputs are drawn on the default stream; the steps run on sp/sc
-    layer = ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas,
-                          producer_pairs=args.producer_pairs)
-    sp = torch.cuda.Stream()
-    sc = torch.cuda.Stream(priority=-1)
+    # Batches in flight: instance i % n (own plan and workspaces, own streams) runs
+    # step i, so one batch's routing, plan and gather overlap the previous batch's
+    # expert FFN. Every step still runs the whole path on its own batch.
+    n_fly = max(1, args.batches_in_flight)
+    layers = [ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas,
+                            producer_pairs=args.producer_pairs) for _ in range(n_fly)]
+    layer = layers[0]
+    sps = [torch.cuda.Stream() for _ in range(n_fly)]
+    scs = [torch.cuda.Stream(priority=-1) for _ in range(n_fly)]
+    sp, sc = sps[0], scs[0]
+    step_i = [0]
 
     def step():
-        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
-                      producer=sp, consumer=sc)
+        j = step_i[0] % n_fly
+        step_i[0] += 1
+        layers[j].forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                          producer=sps[j], consumer=scs[j])
 
-    for _ in range(args.warmup):
+    for _ in range(max(args.warmup, n_fly)):
         step()
     torch.cuda.synchronize()
-    code, detail = layer.status()
-    if code != 0:
-        raise RuntimeError(f"device status {code} detail {detail}")
+    for lay in layers:
+        code, detail = lay.status()
+        if code != 0:
+            raise RuntimeError(f"device status {code} detail {detail}")
 
     # Counts for the algorithmic work of one step (read once, outside the timed region).
     rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
@@ -190,8 +200,12 @@ def gpu_arm(args, rank, world, local_rank):
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
         ev0.record(sp)
+        for s_ in sps[1:]:
+            s_.wait_event(ev0)
         for _ in range(args.steps):
             step()
+        for s_ in sps[1:]:
+            sp.wait_stream(s_)
         ev1.record(sp)
         torch.cuda.synchronize()
         if world > 1:
@@ -200,19 +214,23 @@ def gpu_arm(args, rank, world, local_rank):
     kernel_ms = layer.timings()
     layer.set_timing(False)
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, device="cuda")
-    code, detail = layer.status()
-    if code != 0:
-        raise RuntimeError(f"device status {code} detail {detail} after the timed region")
+    for lay in layers:
+        code, detail = lay.status()
+        if code != 0:
+            raise RuntimeError(f"device status {code} detail {detail} after the timed region")
 
     # ---- stage measurements (outside the timed region) --------------------------------
     stages = stage_times(layer, inp, wl, sp, sc, args)
 
     # ---- e2e through the C ABI with host buffers ----------------------------------------
-    e2e = e2e_arm(layer, inp, wl, sp, sc, args)
+    e2e = e2e_arm(layers, inp, wl, sp, sc, args)
 
     hbm, bf16, bf16_sus, src = _peaks()
     launch = layer.launch_info()
-    prod_avg = kernel_ms[2]
+    # The producer's execution span on the device clock (first CTA start to last CTA
+    # end): with batches in flight, the event pair around a launch also counts the time
+    # the kernel waits for the previous batch's producer to leave the SMs.
+    prod_avg = kernel_ms[6] if kernel_ms[6] > 0 else kernel_ms[2]
     achieved = flops_exec / (prod_avg * 1e-3) / 1e12
     result = {
         "metric": METRIC,
@@ -230,6 +248,7 @@ def gpu_arm(args, rank, world, local_rank):
         "config": {"workload": wl.name, "W": W, "experts_per_rank": wl.L, "topk": k,
                    "tokens_per_rank": T, "d_model": D, "d_ff": F, "tb_M": wl.tb_M,
                    "mgb": wl.mgb, "consumer_ctas": args.consumer_ctas,
+                   "batches_in_flight": n_fly,
                    "schedule": ("fused (copy warp in every producer CTA)" if args.consumer_ctas < 0
                                 else "serial" if args.consumer_ctas == 0
                                 else "overlapped (consumer kernel on its own SMs)"),
@@ -245,9 +264,14 @@ def gpu_arm(args, rank, world, local_rank):
                      "unit": "TFLOP/s", "frac": achieved / bf16_sus,
                      "traffic": producer_traffic(wl.name, args.tokens_per_rank, args.producer_pairs),
                      "peak_source": f"{src} bf16 sustained (kernel timed inside a loop of steps)",
-                     "flops_per_launch": flops_exec, "launch_ms": prod_avg},
+                     "flops_per_launch": flops_exec, "launch_ms": prod_avg,
+                     "launch_ms_source": ("device-clock span of each producer launch (first CTA "
+                                          "start to last CTA end), mean over the timed region"
+                                          if kernel_ms[6] > 0 else
+                                          "CUDA events around each producer launch")},
         "e2e": e2e,
-        "gpu_launches": 10 * args.steps,
+        # route 1 + plan 5 + gather 1 + producer 1 + scale 1, + consumer kernel 1 unless fused
+        "gpu_launches": (9 + (0 if args.consumer_ctas < 0 else 1)) * args.steps,
         "clocks": clk.summary(),
         "stages": stages,
         "work": {"rows_executed": rows_exec, "rows_valid": valid_rows,
@@ -255,11 +279,13 @@ def gpu_arm(args, rank, world, local_rank):
                  "recv_rows": recv_rows},
         "timed_wall_s": wall,
         "kernel_ms_in_timed_region": dict(zip(
-            ["route", "plan", "producer", "consumer", "scale", "gather"], kernel_ms)),
+            ["route", "plan", "producer", "consumer", "scale", "gather", "producer_span"],
+            kernel_ms)),
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    layer.close()
+    for lay in layers:
+        lay.close()
     return result
 
 
@@ -353,7 +379,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     }
 
 
-def e2e_arm(layer, inp, wl, sp, sc, args):
+def e2e_arm(layers, inp, wl, sp, sc, args):
     """Same metric through the public API with pinned host buffers: every step copies its
     inputs in and its output out inside the timed region. The runtime's HostPipeline
     overlaps step i+1's input copy and step i-1's output copy with step i's compute."""
@@ -369,7 +395,7 @@ def e2e_arm(layer, inp, wl, sp, sc, args):
     h2d = sum(t.numel() * t.element_size() for t in hx) + hl.numel() * 4 + \
         (0 if hf is None else hf.numel() * 4)
     d2h = sum(t.numel() * t.element_size() for t in hout)
-    pipe = HostPipeline(layer, sp, sc, forced=hf is not None)
+    pipe = HostPipeline(layers, sp, sc, forced=hf is not None)
 
     def step(start_after=None):
         pipe.step(hx, hl, hf, hout, inp.w_gate, inp.w_up, inp.w_down, start_after=start_after)
@@ -474,6 +500,9 @@ def main():
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batches-in-flight", type=int, default=2,
+                    help="layer instances (own plan and workspaces) that take steps in turn, so "
+                         "one batch's routing, plan and gather overlap the previous batch's FFN")
     ap.add_argument("--producer-pairs", type=int, default=1, choices=[0, 1],
                     help="1: the CTA-pair producer (clusters of two, tcgen05 cta_group::2)")
     ap.add_argument("--ccta-sweep", type=lambda v: [int(x) for x in v.split(",") if x],

@@ -250,9 +250,12 @@ int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count)
  * recorded on the stream each kernel ran on: the mean over the calls made since
  * timing was last enabled (the most recent 64 of them). Synchronises on those
  * events. Order: [0] route, [1] plan (all plan kernels and the gather),
- * [2] producer, [3] consumer, [4] scale, [5] gather only. A slot with no
- * measurement is -1. Instrumentation only: events are recorded only while
- * enabled, and enabling resets the counts. */
+ * [2] producer, [3] consumer, [4] scale, [5] gather only, and [6] the producer's
+ * execution span on the device clock (its first CTA's start to its last CTA's end;
+ * unlike [2] it excludes time spent queued behind other kernels, for example those
+ * of another batch in flight). A slot with no measurement is -1. Instrumentation
+ * only: events and spans are recorded only while enabled, and enabling resets the
+ * counts. */
 int moe_set_timing(moe_plan *plan, int enable);
 int moe_timings(moe_plan *plan, float *ms, int n);
 

@@ -13,8 +13,9 @@ from tile_signaled_grouped_gb300.runtime import ExpertCombine, HostPipeline  # n
 from tile_signaled_grouped_gb300.workloads import get_workload, make_inputs  # noqa: E402
 
 
+@pytest.mark.parametrize("n_layers", [1, 2])
 @pytest.mark.parametrize("name", ["tiny", "a100_like"])
-def test_pipelined_steps_equal_plain_forward(name):
+def test_pipelined_steps_equal_plain_forward(name, n_layers):
     base = get_workload(name)
     sets = [make_inputs(get_workload(name, seed=s), device="cuda", with_weights=s == 0)
             for s in (0, 3, 5)]
@@ -31,9 +32,9 @@ def test_pipelined_steps_equal_plain_forward(name):
         torch.cuda.synchronize()
         assert ref_layer.status() == (0, 0)
         want.append([t.cpu().clone() for t in out])
-    layer = mk()
+    layers = [mk() for _ in range(n_layers)]  # 2: batches in flight, each on its own instance
     forced = sets[0].forced_ids is not None
-    pipe = HostPipeline(layer, forced=forced)
+    pipe = HostPipeline(layers if n_layers > 1 else layers[0], forced=forced)
     order = [0, 1, 2, 1, 0, 2, 2]
     houts = []
     for i in order:
@@ -47,7 +48,7 @@ def test_pipelined_steps_equal_plain_forward(name):
         houts.append(hout)
     pipe.done_event().synchronize()
     torch.cuda.synchronize()
-    assert layer.status() == (0, 0)
+    assert all(lay.status() == (0, 0) for lay in layers)
     for i, hout in zip(order, houts):
         for got, ref in zip(hout, want[i]):
             assert torch.equal(got, ref), f"step with input set {i}"

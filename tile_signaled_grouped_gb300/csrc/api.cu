@@ -37,6 +37,7 @@ struct moe_plan {
   cudaEvent_t ev_ready, ev_join;
   cudaEvent_t ev_t0[kTSlots][kTRing], ev_t1[kTSlots][kTRing];
   int nrec[kTSlots];  // measurements recorded since timing was enabled
+  int nspan;          // producer kernel spans recorded since timing was enabled
   bool timing;
 };
 
@@ -116,6 +117,7 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_SCALE_SRC] = W * (size_t)d.T * d.k;
   n[PA_PAIR] = 4 * W * NMM;
   n[PA_PAIR_UNIT_BEGIN] = n[PA_UNIT_BEGIN];
+  n[PA_SPANS] = 4 * kSpanRing;
   size_t pos = 0;
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;
@@ -372,6 +374,13 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
   ProducerArgs pa;
   std::memset(&pa, 0, sizeof(pa));
   pa.p = dev_plan(p);
+  if (p->timing) {  // the producer folds its execution span into a zeroed ring slot
+    unsigned long long* ring =
+        reinterpret_cast<unsigned long long*>(p->plan_ws + p->offsets[PA_SPANS]);
+    pa.span = ring + 2 * (p->nspan % kSpanRing);
+    CUDA_TRY(cudaMemsetAsync(pa.span, 0, 2 * sizeof(unsigned long long), sp));
+    p->nspan++;
+  }
   for (int r = 0; r < d.W; ++r) {
     uint8_t* ws = p->rank_ws[r];
     const void* X = ws + p->rl.x_off;
@@ -499,6 +508,7 @@ int moe_set_timing(moe_plan* p, int enable) {
   if (p == nullptr) return MOE_ERR_ARG;
   p->timing = enable != 0;
   for (int i = 0; i < kTSlots; ++i) p->nrec[i] = 0;
+  p->nspan = 0;
   return MOE_OK;
 }
 
@@ -517,6 +527,22 @@ int moe_timings(moe_plan* p, float* ms, int n) {
       sum += v;
     }
     ms[i] = (float)(sum / m);
+  }
+  if (n > kTSlots) {  // producer kernel span on the device clock
+    ms[kTSlots] = -1.f;
+    const int m = std::min(p->nspan, kSpanRing);
+    if (m > 0) {
+      CUDA_TRY(cudaDeviceSynchronize());
+      unsigned long long ring[2 * kSpanRing];
+      CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
+                          cudaMemcpyDeviceToHost));
+      double sum = 0.0;
+      for (int j = 0; j < m; ++j) {
+        const int q = (p->nspan - 1 - j) % kSpanRing;
+        sum += (double)(ring[2 * q + 1] - ~ring[2 * q]) * 1e-6;
+      }
+      ms[kTSlots] = (float)(sum / m);
+    }
   }
   return MOE_OK;
 }

@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
+  if (threadIdx.x == 0) span_begin(a.span);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -392,6 +393,7 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
     __syncwarp();
     tmem_dealloc(tmem_base, 2 * kAccCols);
   }
+  if (threadIdx.x == 0) span_end(a.span);
 }
 
 }  // namespace

@@ -311,6 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
   cluster_sync_all();  // both CTAs: barriers initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
+  if (threadIdx.x == 0) span_begin(a.span);
 
   if (FUSED && warp == kCopyWarp) {
     // ------------------------------------------------------------ combine copy
@@ -586,6 +587,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
     __syncwarp();
     tmem_dealloc_pair(tmem_base, 2 * kPAccCols);
   }
+  if (threadIdx.x == 0) span_end(a.span);
 }
 
 }  // namespace

@@ -30,6 +30,7 @@ constexpr size_t kConsumerSmemTail = 12 * 1024;  // barriers, counters and recor
 constexpr size_t kConsumerSmem = (size_t)kChunkSlots * kChunkBytes + kConsumerSmemTail;
 constexpr int kSegRec = 8;                   // ints per consumer segment record
 constexpr int kMaxSegChunks = 256;           // copy chunks one segment may have
+constexpr int kSpanRing = 64;                // producer kernel spans kept while timing
 
 // ---------------------------------------------------------------------------
 // Dimensions derived from a configuration (host and device).
@@ -64,6 +65,7 @@ enum PlanArray {
   PA_SEG_REC, PA_GROUP_NCHUNK,
   PA_XSRC, PA_SCALE_SRC,
   PA_PAIR, PA_PAIR_UNIT_BEGIN,
+  PA_SPANS,  // [kSpanRing][2] u64: producer kernel spans recorded while timing is on
   PA_COUNT
 };
 
@@ -115,6 +117,9 @@ struct ProducerArgs {
   __nv_bfloat16* h[MOE_MAX_RANKS];
   __nv_bfloat16* y[MOE_MAX_RANKS];
   __nv_bfloat16* recv[MOE_MAX_RANKS];  // receive buffers (the fused pair producer copies into them)
+  // Timing on: the kernel's execution span on the device clock, {~first CTA start,
+  // last CTA end}, both folded in with atomicMax into a slot the host zeroed.
+  unsigned long long* span;
   DevPlan p;
   int lag;  // scheduling units between a unit's GEMM1 tiles and its GEMM2 tiles
 };
@@ -152,6 +157,14 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Producer kernel span (timing on): the first CTA's start and the last CTA's end.
+__device__ __forceinline__ void span_begin(unsigned long long* span) {
+  if (span != nullptr) atomicMax(span, ~globaltimer());
+}
+__device__ __forceinline__ void span_end(unsigned long long* span) {
+  if (span != nullptr) atomicMax(span + 1, globaltimer());
 }
 
 // First error wins; detail is written by the same winner.

@@ -19,7 +19,11 @@
 namespace moe {
 namespace {
 
-constexpr int kMaxLocal = 256;  // experts per rank handled by the per-rank kernel
+// The two per-rank / single-CTA plan kernels run with 256 threads and size their
+// shared arrays to the layer (L experts per rank, W ranks), so that they fit on an SM
+// beside a running producer CTA (which leaves about 26K registers and 4 KB of
+// shared memory): the plan of one batch can then overlap the FFN of another.
+constexpr int kPlanThreads = 256;
 
 __device__ __forceinline__ int roundup(int a, int m) { return (a + m - 1) / m * m; }
 
@@ -114,14 +118,26 @@ __device__ __forceinline__ int last_le(const int* a, int n, int v) {
   return lo;
 }
 
+// Dynamic shared memory of plan_rank_kernel: 7 arrays of L ints, 2 of L * W.
+__host__ __device__ inline size_t rank_smem_bytes(int L, int W) {
+  return (size_t)(7 * L + 2 * L * W) * sizeof(int);
+}
+
 // One CTA per owner rank o: layout X_e, schedule S, combine plan, segments.
-__global__ void __launch_bounds__(1024) plan_rank_kernel(DevPlan p) {
+__global__ void __launch_bounds__(kPlanThreads) plan_rank_kernel(DevPlan p) {
   const Dims d = p.d;
   const int o = blockIdx.x;
   const int tid = threadIdx.x, nt = blockDim.x;
-  __shared__ int s_rows_alloc[kMaxLocal], s_nb[kMaxLocal], s_nrb[kMaxLocal], s_estart[kMaxLocal];
-  __shared__ int s_order[kMaxLocal], s_rpre[kMaxLocal], s_lpre[kMaxLocal];
-  __shared__ int s_gs[kMaxLocal * MOE_MAX_RANKS], s_cnt[kMaxLocal * MOE_MAX_RANKS];
+  extern __shared__ int s_dyn[];
+  int* s_rows_alloc = s_dyn;
+  int* s_nb = s_rows_alloc + d.L;
+  int* s_nrb = s_nb + d.L;
+  int* s_estart = s_nrb + d.L;
+  int* s_order = s_estart + d.L;
+  int* s_rpre = s_order + d.L;
+  int* s_lpre = s_rpre + d.L;
+  int* s_gs = s_lpre + d.L;         // [L][W]
+  int* s_cnt = s_gs + d.L * d.W;    // [L][W]
   __shared__ int scratch[33];
   __shared__ int s_NB, s_R;
 
@@ -352,7 +368,7 @@ __device__ __forceinline__ int rr_unit(const int* len, int W, int o, int q, int 
 // chunks of kTileGroup tiles round-robin over the ranks, each rank in its S order;
 // then the local tiles the same way), its scheduling units, and the consumer's
 // segment order (following the tile order).
-__global__ void __launch_bounds__(1024) plan_order_kernel(DevPlan p) {
+__global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
   const Dims d = p.d;
   const int tid = threadIdx.x, nt = blockDim.x;
   __shared__ int scratch[33];
@@ -646,10 +662,10 @@ cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s) {
   plan_bitmap_kernel<<<(ntok + 255) / 256, 256, 0, s>>>(p, ids);
   const int warps = d.E * d.W;
   plan_count_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
-  plan_rank_kernel<<<d.W, 1024, 0, s>>>(p);
+  plan_rank_kernel<<<d.W, kPlanThreads, rank_smem_bytes(d.L, d.W), s>>>(p);
   const int na = d.W * d.T * d.k;
   plan_scatter_kernel<<<(na + 255) / 256, 256, 0, s>>>(p, ids);
-  plan_order_kernel<<<1, 1024, 0, s>>>(p);
+  plan_order_kernel<<<1, kPlanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

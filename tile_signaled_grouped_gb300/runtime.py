@@ -177,48 +177,64 @@ class ExpertCombine:
         capi.moe_set_timing(self.plan, enable)
 
     def timings(self):
-        return capi.moe_timings(self.plan, 6)
+        """[route, plan, producer, consumer, scale, gather, producer span] in ms (-1: none)."""
+        return capi.moe_timings(self.plan, 7)
 
 
 class HostPipeline:
-    """Steps of one layer fed from and returned to pinned host memory, with the copies
-    overlapped with compute: step i+1's inputs are copied in while step i computes,
-    and step i's outputs are copied out while step i+1 computes.
+    """Steps of one MoE layer fed from and returned to pinned host memory, with the
+    copies overlapped with compute: step i+1's inputs are copied in while step i
+    computes, and step i's outputs are copied out while step i+1 computes.
 
     Two sets of device inputs (tokens, logits, forced ids) and two sets of outputs
     alternate; one copy stream per direction. Events order everything on the GPU:
     a set's inputs are overwritten only after the plan build of the step that read
     them, and its outputs only after their copy to the host finished. Every step
     still moves all of its input and output bytes; nothing is cached across steps.
+
+    `layer` may also be a list of ExpertCombine instances of the same layer (same
+    shape, own workspaces): step i then runs on instance i % len, on its own streams,
+    so the routing, plan and gather of one batch overlap the expert FFN of the
+    previous one (batches in flight).
     """
 
-    def __init__(self, layer: ExpertCombine, producer=None, consumer=None, forced=False):
-        dev = layer.device
-        W, T, D, E, k = layer.W, layer.T, layer.D, layer.W * layer.L, layer.k
-        self.layer = layer
-        self.sp = producer or torch.cuda.Stream(device=dev)
-        self.sc = consumer or torch.cuda.Stream(device=dev, priority=-1)
+    def __init__(self, layer, producer=None, consumer=None, forced=False):
+        self.layers = list(layer) if isinstance(layer, (list, tuple)) else [layer]
+        lay0 = self.layers[0]
+        dev = lay0.device
+        W, T, D, E, k = lay0.W, lay0.T, lay0.D, lay0.W * lay0.L, lay0.k
+        n = max(2, len(self.layers))
+        self.nbuf = n
+        self.sp = [producer or torch.cuda.Stream(device=dev)] + \
+            [torch.cuda.Stream(device=dev) for _ in self.layers[1:]]
+        self.sc = [consumer or torch.cuda.Stream(device=dev, priority=-1)] + \
+            [torch.cuda.Stream(device=dev, priority=-1) for _ in self.layers[1:]]
         self.s_in = torch.cuda.Stream(device=dev)
         self.s_out = torch.cuda.Stream(device=dev)
         self.x = [[torch.empty(T, D, dtype=torch.bfloat16, device=dev) for _ in range(W)]
-                  for _ in range(2)]
-        self.logits = [torch.empty(W, T, E, dtype=torch.float32, device=dev) for _ in range(2)]
+                  for _ in range(n)]
+        self.logits = [torch.empty(W, T, E, dtype=torch.float32, device=dev) for _ in range(n)]
         self.forced = [torch.empty(W, T, k, dtype=torch.int32, device=dev) if forced else None
-                       for _ in range(2)]
+                       for _ in range(n)]
         self.out = [[torch.empty(T, D, dtype=torch.bfloat16, device=dev) for _ in range(W)]
-                    for _ in range(2)]
-        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+                    for _ in range(n)]
+        ev = lambda: [torch.cuda.Event() for _ in range(n)]
         self.ev_in, self.ev_free, self.ev_done, self.ev_out = ev(), ev(), ev(), ev()
-        self.started = [False, False]
+        self.started = [False] * n
         self.i = 0
+
+    @property
+    def sp0(self):
+        return self.sp[0]
 
     def step(self, hx, hlogits, hforced, hout, w_gate, w_up, w_down, start_after=None):
         """Enqueue one step. hx: W pinned [T, D] bf16; hlogits: pinned [W, T, E] fp32;
         hforced: pinned [W, T, k] int32 or None; hout: W pinned [T, D] bf16 written when
         the step's output copy completes (after self.done_event() of this step).
         start_after: an event the first copy must follow (for timing)."""
-        b = self.i % 2
-        lay = self.layer
+        b = self.i % self.nbuf
+        li = self.i % len(self.layers)
+        lay, sp, sc = self.layers[li], self.sp[li], self.sc[li]
         if start_after is not None:
             self.s_in.wait_event(start_after)
         if self.started[b]:
@@ -230,15 +246,15 @@ class HostPipeline:
             if hforced is not None:
                 self.forced[b].copy_(hforced, non_blocking=True)
         self.ev_in[b].record(self.s_in)
-        self.sp.wait_event(self.ev_in[b])
-        lay.route(self.logits[b], self.forced[b] if hforced is not None else None, self.sp)
-        lay.plan_build(self.x[b], stream=self.sp)
-        self.ev_free[b].record(self.sp)
-        lay.expert_combine(w_gate, w_up, w_down, self.sp, self.sc)
+        sp.wait_event(self.ev_in[b])
+        lay.route(self.logits[b], self.forced[b] if hforced is not None else None, sp)
+        lay.plan_build(self.x[b], stream=sp)
+        self.ev_free[b].record(sp)
+        lay.expert_combine(w_gate, w_up, w_down, sp, sc)
         if self.started[b]:
-            self.sp.wait_event(self.ev_out[b])
-        lay.scale(stream=self.sp, out=self.out[b])
-        self.ev_done[b].record(self.sp)
+            sp.wait_event(self.ev_out[b])
+        lay.scale(stream=sp, out=self.out[b])
+        self.ev_done[b].record(sp)
         self.s_out.wait_event(self.ev_done[b])
         with torch.cuda.stream(self.s_out):
             for h, o in zip(hout, self.out[b]):
@@ -250,4 +266,4 @@ class HostPipeline:
 
     def done_event(self):
         """Event completed when the last enqueued step's outputs are on the host."""
-        return self.ev_out[(self.i - 1) % 2]
+        return self.ev_out[(self.i - 1) % self.nbuf]
