@@ -70,6 +70,7 @@ def test_workspace_sizes_follow_the_worst_case(lib):
     dict(W=0), dict(W=9), dict(L=0), dict(topk=0), dict(topk=9, W=1, L=8), dict(T=0),
     dict(d_model=100), dict(d_ff=64), dict(tb_M=96), dict(mgb=0), dict(consumer_ctas=-1),
     dict(producer_pairs=2), dict(producer_pairs=-1),
+    dict(consumer_ctas=-1, producer_pairs=0), dict(consumer_ctas=-2, producer_pairs=1),
 ])
 def test_invalid_configurations_are_rejected(lib, bad):
     with pytest.raises(capi.MoeError, match="MOE_ERR_ARG"):
@@ -126,3 +127,18 @@ def test_plan_arrays_are_aligned(lib, shape):
                                                          "MOE_PLAN_GROUP_SIG"):
             off, _ = capi.moe_field(c, v)
             assert off % 256 == 0, (name, off)
+
+
+def test_fused_schedule_is_a_valid_configuration(lib):
+    """consumer_ctas = MOE_CONSUMER_FUSED needs the pair producer; then it is accepted."""
+    assert capi.MOE_CONSUMER_FUSED == -1
+    pb, rb, _ = capi.moe_workspace_size(_cfg(consumer_ctas=capi.MOE_CONSUMER_FUSED,
+                                             producer_pairs=1))
+    assert pb > 0 and rb > 0
+
+
+def test_plan_calls_reject_a_null_plan(lib):
+    lib_ = capi.lib()
+    assert lib_.moe_set_schedule(None, 0, 1) == capi.MOE_ERR_ARG
+    assert lib_.moe_launch_info(None, None, None, None, None) == capi.MOE_ERR_ARG
+    assert lib_.moe_status(None, None, None, None) == capi.MOE_ERR_ARG

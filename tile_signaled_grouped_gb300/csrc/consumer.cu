@@ -9,7 +9,8 @@
 // Perseus summary (papercache.org), section 4.1, Algorithm 1: data moves without
 // signals; one fence then precedes the signals of a whole destination group.
 //
-// GB300 form: each segment is cut into chunks of rpc rows (up to 40 KB); the
+// GB300 form (the body is combine_copy.cuh, shared with the copy warp of the fused
+// pair producer): each segment is cut into chunks of rpc rows (up to 20 KB); the
 // chunks of all segments, in the producer's tile order, are dealt round-robin to
 // the consumer CTAs, so every CTA follows production and the last segment is
 // copied by all of them. A CTA is one warp: the lanes poll the flags of a chunk's
@@ -48,7 +49,7 @@ cudaError_t preload_consumer() {
 }
 
 cudaError_t launch_consumer(const ConsumerArgs& a, int grid, cudaStream_t s) {
-  // 120 KB of shared memory per CTA also keeps a consumer CTA from sharing an SM
+  // 132 KB of shared memory per CTA also keeps a consumer CTA from sharing an SM
   // with a producer CTA or another consumer CTA: the kernels run on disjoint SMs.
   consumer_kernel<<<grid, kConsumerThreads, kConsumerSmem, s>>>(a);
   return cudaGetLastError();

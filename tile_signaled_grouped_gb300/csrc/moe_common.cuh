@@ -24,7 +24,7 @@ constexpr int kTileGroup = 32;   // tiles per scheduling unit (weight reuse in L
 constexpr int kProducerThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kConsumerThreads = 32;         // one warp: lane 0 drives the bulk copies
 constexpr int kChunkBytes = 20 * 1024;       // consumer copy chunk (one shared-memory slot)
-constexpr int kChunkSlots = 6;               // 120 KB: keeps one consumer CTA alone on its SM
+constexpr int kChunkSlots = 6;               // 120 KB (+ the tail): one consumer CTA per SM
 constexpr int kLoadsInFlight = 4;            // consumer bulk loads outstanding at most
 constexpr size_t kConsumerSmemTail = 12 * 1024;  // barriers, counters and records after the slots
 constexpr size_t kConsumerSmem = (size_t)kChunkSlots * kChunkBytes + kConsumerSmemTail;
