@@ -172,3 +172,30 @@ def test_route_and_plan_for_every_expert_count(wl):
     P.check_plan(layer, wl, plan, ids, w)
     P.check_order(layer, wl, plan)
     layer.close()
+
+
+@pytest.mark.parametrize("mode", ["overlap", "fused"])
+def test_layout_changes_between_builds(mode):
+    """The gather leaves rows that were zero and stay zero untouched; with the routing
+    changing from build to build (rows turn from token rows into padding and back),
+    every build still has exactly its tokens' rows, zero padding rows and exact
+    outputs."""
+    base = SMALL[0]  # W=3, tb_M=64: many padding rows
+    sets = [P.inputs_for(dataclasses.replace(base, seed=s)) for s in (0, 11, 0, 23)]
+    w = sets[0]
+    cc = 4 if mode == "overlap" else -1
+    from tile_signaled_grouped_gb300.runtime import ExpertCombine
+    layer = ExpertCombine(base.W, base.L, base.topk, base.T, base.d_model, base.d_ff,
+                          base.tb_M, base.mgb, cc, 0, 1)
+    sp, sc = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    for inp in sets:
+        inp.w_gate, inp.w_up, inp.w_down = w.w_gate, w.w_up, w.w_down
+        torch.cuda.synchronize()
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                      producer=sp, consumer=sc)
+        torch.cuda.synchronize()
+        assert layer.status() == (0, 0)
+        ids, wt, plan = P.oracle_plan(base, inp)
+        P.check_plan(layer, base, plan, ids, wt)
+        P.check_layout_and_outputs(layer, base, inp, plan, ids, wt)
+    layer.close()

@@ -38,6 +38,7 @@ struct moe_plan {
   cudaEvent_t ev_t0[kTSlots][kTRing], ev_t1[kTSlots][kTRing];
   int nrec[kTSlots];  // measurements recorded since timing was enabled
   int nspan;          // producer kernel spans recorded since timing was enabled
+  bool xprev_ready;   // PA_XPREV holds the rows' contents (set by the first plan build)
   bool timing;
 };
 
@@ -118,6 +119,7 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_PAIR] = 4 * W * NMM;
   n[PA_PAIR_UNIT_BEGIN] = n[PA_UNIT_BEGIN];
   n[PA_SPANS] = 4 * kSpanRing;
+  n[PA_XPREV] = W * (size_t)d.RM;
   size_t pos = 0;
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;
@@ -346,6 +348,10 @@ int moe_plan_build(moe_plan* p, const int32_t* ids, const void* const* x, moe_st
   for (int r = 0; r < p->d.W; ++r) {
     xs[r] = static_cast<const __nv_bfloat16*>(x[r]);
     xb[r] = reinterpret_cast<__nv_bfloat16*>(p->rank_ws[r] + p->rl.x_off);
+  }
+  if (!p->xprev_ready) {  // first build: every X row's content is unknown (0xFEFEFEFE)
+    CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_XPREV], 0xFE, p->counts[PA_XPREV] * 4, s));
+    p->xprev_ready = true;
   }
   tstart(p, kTGather, s);
   CUDA_TRY(launch_gather(dp, xs, xb, p->num_sms, s));

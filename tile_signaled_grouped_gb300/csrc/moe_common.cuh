@@ -66,6 +66,7 @@ enum PlanArray {
   PA_XSRC, PA_SCALE_SRC,
   PA_PAIR, PA_PAIR_UNIT_BEGIN,
   PA_SPANS,  // [kSpanRing][2] u64: producer kernel spans recorded while timing is on
+  PA_XPREV,  // [W][RM] what each X row held after the last gather: token, -1 zero, else unknown
   PA_COUNT
 };
 

@@ -594,7 +594,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
 // Layout gather: X rows of every owner from its tokens' rows, zero rows elsewhere
 // (padding, block tails, and up to the next 128-row boundary). One warp per row,
 // over the rows that exist (their count is read on the device); each lane keeps
-// up to 8 independent 16-byte loads in flight.
+// up to 8 independent 16-byte loads in flight. A row that is to be zero and was
+// already zero after the previous gather (PA_XPREV) is left alone: padding-heavy
+// layouts keep most of their zero rows from one step to the next.
 struct GatherPtrs {
   const __nv_bfloat16* x[MOE_MAX_RANKS];
   __nv_bfloat16* xb[MOE_MAX_RANKS];
@@ -619,7 +621,12 @@ __global__ void layout_gather_kernel(DevPlan p, const __grid_constant__ GatherPt
     const int r = gw - (o > 0 ? end[o - 1] : 0);
     const int rows = p.a[PA_RANK_ROWS][o];
     const int src = r < rows ? p.a[PA_XSRC][(size_t)o * d.RM + r] : -1;
+    int32_t* prev = p.a[PA_XPREV] + (size_t)o * d.RM + r;
+    const int before = *prev;
     uint4* dst = reinterpret_cast<uint4*>(g.xb[o] + (size_t)r * d.D);
+    if (src < 0 && before == -1) continue;  // still a zero row
+    __syncwarp();
+    if (lane == 0 && before != src) *prev = src;
     if (src >= 0) {
       const int s = src / d.T, t = src % d.T;
       const uint4* sp = reinterpret_cast<const uint4*>(g.x[s] + (size_t)t * d.D);
