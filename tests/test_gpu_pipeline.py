@@ -13,16 +13,16 @@ from tile_signaled_grouped_gb300.runtime import ExpertCombine, HostPipeline  # n
 from tile_signaled_grouped_gb300.workloads import get_workload, make_inputs  # noqa: E402
 
 
-@pytest.mark.parametrize("n_layers", [1, 2])
+@pytest.mark.parametrize("n_layers,cctas", [(1, 4), (2, 4), (2, -1)])
 @pytest.mark.parametrize("name", ["tiny", "a100_like"])
-def test_pipelined_steps_equal_plain_forward(name, n_layers):
+def test_pipelined_steps_equal_plain_forward(name, n_layers, cctas):
     base = get_workload(name)
     sets = [make_inputs(get_workload(name, seed=s), device="cuda", with_weights=s == 0)
             for s in (0, 3, 5)]
     w = sets[0]  # one set of expert weights for every step
     torch.cuda.synchronize()  # inputs are drawn on the default stream; the layer runs on others
     mk = lambda: ExpertCombine(base.W, base.L, base.topk, base.T, base.d_model, base.d_ff,
-                               base.tb_M, base.mgb, consumer_ctas=4)
+                               base.tb_M, base.mgb, consumer_ctas=cctas)
     ref_layer = mk()
     sp, sc = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
     want = []
@@ -66,11 +66,11 @@ def test_tuned_schedule_keeps_results_exact():
     torch.cuda.synchronize()
     layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb,
                           consumer_ctas=4)
-    cands = ((0, 1), (4, 1), (2, 2), (8, 3))
+    cands = ((-1, 1), (0, 1), (4, 1), (2, 2), (8, 3))
     cc, mgb, times = layer.tune(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits,
                                 inp.forced_ids, candidates=cands, steps=2)
     assert (cc, mgb) in times and set(times) == set(cands)
-    assert layer.launch_info()[1] == cc
+    assert layer.launch_info()[1] == max(cc, 0)  # the fused schedule runs no consumer CTAs
     sp = torch.cuda.Stream()
     layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
                   producer=sp, consumer=torch.cuda.Stream(priority=-1))
