@@ -52,6 +52,11 @@ design notes of the repository):
       Here the operands are bf16, so the hidden activation h = SiLU(g) * u, being
       the second GEMM's input, is rounded to bf16 (to nearest, ties to even)
       before W_down is applied. Everything else is float64.
+  R14 The gate ([TileMoE] 2.1: a small gating network; 2.2 step 1: every rank
+      gates its own tokens) is one bias-free linear layer whose weights
+      w_router [E, D] every rank holds alike: logits_s[t] = w_router x_s[t]. Its
+      operands are half precision like the expert GEMMs' (R11); the scores are
+      float64 sums of the bf16 values here.
 """
 from __future__ import annotations
 
@@ -60,8 +65,9 @@ import dataclasses
 import numpy as np
 
 __all__ = [
-    "softmax", "silu", "round_bf16", "route", "Plan", "build_plan", "expert_ffn", "layout_rows",
-    "rank_outputs", "buffer_row_outputs", "combine", "scale", "forward", "padding_bound",
+    "softmax", "silu", "round_bf16", "route", "gate_logits", "gate", "Plan", "build_plan",
+    "expert_ffn", "layout_rows", "rank_outputs", "buffer_row_outputs", "combine", "scale",
+    "forward", "padding_bound",
 ]
 
 
@@ -96,6 +102,22 @@ def route(logits, k: int, forced_ids=None):
         ids = np.asarray(forced_ids, dtype=np.int64)
     w = np.take_along_axis(p, ids, axis=-1)
     return ids.astype(np.int64), w
+
+
+def gate_logits(x, w_router) -> np.ndarray:
+    """Gate scores of every token: logits[s][t][e] = sum_c x[s][t][c] * w_router[e][c].
+
+    x: [W, T, D] token rows; w_router: [E, D] (nn.Linear layout), shared by the
+    ranks (reading R14). float64 sums of the given values.
+    """
+    xs = np.asarray(x, dtype=np.float64)
+    wr = np.asarray(w_router, dtype=np.float64)
+    return xs @ wr.T
+
+
+def gate(x, w_router, k: int, forced_ids=None):
+    """Routing from the token rows: the gate scores (gate_logits), then route()."""
+    return route(gate_logits(x, w_router), k, forced_ids)
 
 
 # --------------------------------------------------------------------------

@@ -68,6 +68,45 @@ def test_route_brute_force_and_forced_ids():
     assert w[0, 0, 0] < 1 and w[0, 0, 1] < 1
 
 
+def test_gate_logits_operand_roles_and_brute_force():
+    rng = np.random.default_rng(7)
+    # Square router, token c = unit vector e_c: score of expert e is w_router[e][c]
+    # (a transposed router would give w_router[c][e]).
+    wr = rng.standard_normal((6, 6))
+    x = np.eye(6)[None]
+    lg = O.gate_logits(x, wr)
+    assert lg.shape == (1, 6, 6)
+    for c in range(6):
+        for e in range(6):
+            assert lg[0, c, e] == wr[e, c]
+    # Tiny non-square case against an exactly rounded sum.
+    x = rng.standard_normal((2, 3, 5))
+    wr = rng.standard_normal((4, 5))
+    lg = O.gate_logits(x, wr)
+    assert lg.shape == (2, 3, 4)
+    for s in range(2):
+        for t in range(3):
+            for e in range(4):
+                assert abs(lg[s, t, e] - math.fsum(x[s, t, c] * wr[e, c] for c in range(5))) < 1e-12
+
+
+def test_gate_closed_form_routing():
+    # One token (1, 0); router column 0 = (0, ln3, ln3, 0): the scores of the
+    # closed-form routing case above, whatever column 1 holds.
+    wr = np.array([[0.0, 5.0], [math.log(3.0), -2.0], [math.log(3.0), 7.0], [0.0, 1.0]])
+    ids, w = O.gate(np.array([[[1.0, 0.0]]]), wr, 2)
+    assert ids[0, 0].tolist() == [1, 2]
+    np.testing.assert_allclose(w[0, 0], [3 / 8, 3 / 8], rtol=1e-12)
+    # The identity router routes each token to its own largest entries.
+    x = np.array([[[0.5, -1.0, 2.0, 0.25], [3.0, 3.0, -4.0, 1.0]]])
+    ids, _ = O.gate(x, np.eye(4), 2)
+    assert ids[0].tolist() == [[2, 0], [0, 1]]
+    # Prescribed ids keep the probabilities of the computed scores.
+    ids, w = O.gate(np.array([[[1.0, 0.0]]]), wr, 2, forced_ids=np.array([[[3, 1]]]))
+    assert ids[0, 0].tolist() == [3, 1]
+    np.testing.assert_allclose(w[0, 0], [1 / 8, 3 / 8], rtol=1e-12)
+
+
 # ---------------------------------------------------------------- FFN
 
 def test_silu_special_values():

@@ -29,11 +29,12 @@
 // combine copy in one more warp (the standalone consumer's body with one chunk
 // slot), so no SM is set aside for the consumer; the pipeline keeps six stages.
 //
-// Waits. A GEMM2 task waits (bounded by timeout_ns) until its tile's GEMM1 tiles
-// are counted; on expiry it records MOE_DEV_TIMEOUT and still completes the task
-// (its result is void), so the two CTAs never disagree on the task sequence; the
-// leader stops taking tickets as soon as the status word is set. Every other wait
-// depends only on the pair's own progress and is bounded by timeout_ns + 4 s.
+// Waits. The scheduler posts a GEMM2 task once its rows' GEMM1 tiles are counted
+// (a wait bounded by timeout_ns); on expiry it records MOE_DEV_TIMEOUT and posts the
+// task anyway (its result is void), so the two CTAs never disagree on the task
+// sequence; the leader stops taking tickets as soon as the status word is set.
+// Every other wait depends only on the pair's own progress and is bounded by
+// timeout_ns + 4 s.
 // The CTAs meet in a cluster barrier only at the start (barriers and TMEM ready
 // in both) and at the end (every MMA drained, every copy landed), then free TMEM.
 #include "combine_copy.cuh"
@@ -605,6 +606,7 @@ cudaError_t preload_producer_pair() {
                               (int)PairCfg<true>::kSmem);
 }
 
+namespace {
 template <bool FUSED>
 int max_clusters() {
   cudaLaunchConfig_t cfg = {};
@@ -618,6 +620,7 @@ int max_clusters() {
   }
   return n;
 }
+}  // namespace
 
 int producer_pair_max_clusters(bool fused) {
   return fused ? max_clusters<true>() : max_clusters<false>();
