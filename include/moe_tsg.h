@@ -120,6 +120,25 @@ void moe_plan_destroy(moe_plan *plan);
 int moe_route(moe_plan *plan, const float *logits, const int32_t *forced_ids,
               int32_t *topk_ids, float *topk_w, moe_stream_t stream);
 
+/* Gate from the token rows (TileMoE notes section 2.1: a small gating network;
+ * 2.2 step 1: every rank gates its own tokens), in one kernel: the router's
+ * scores logits[s][t][e] = sum_c x_s[t][c] * w_router[e][c] (bf16 operands, fp32
+ * sums on the tensor cores), then the routing of moe_route on those scores.
+ *  x:          W pointers, rank s's tokens [T][D] bf16, 16-byte aligned.
+ *  w_router:   [E][D] bf16 (nn.Linear layout), one copy shared by every rank,
+ *              16-byte aligned.
+ *  forced_ids, topk_ids, topk_w: as moe_route.
+ *  logits:     NULL, or out [W][T][E] fp32: the scores the routing used.
+ *  splits:     0 picks the K split; 1, 2, 4 or 8 forces it (that many CTAs of one
+ *              cluster share a 128-token tile, each summing a range of D; their
+ *              partial sums are added in a fixed order, so a given split gives
+ *              the same bits on every call).
+ * E <= 256; larger E, or a split the GPU cannot hold, gives MOE_ERR_UNSUPPORTED.
+ * The caller owns every buffer. Timed in slot [0] of moe_timings. */
+int moe_gate(moe_plan *plan, const void *const *x, const void *w_router,
+             const int32_t *forced_ids, int32_t *topk_ids, float *topk_w, float *logits,
+             int splits, moe_stream_t stream);
+
 /* Expert problem construction and combine plan (TileMoE notes section 4.2, 4.4
  * Algorithm 1, 4.5, 5.2) for all ranks, then the layout gather that fills each
  * owner's expert input X with its tokens' rows (zero rows for padding).
@@ -249,7 +268,7 @@ int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count)
 /* Device time in ms of the kernels the calls enqueue, measured with CUDA events
  * recorded on the stream each kernel ran on: the mean over the calls made since
  * timing was last enabled (the most recent 64 of them). Synchronises on those
- * events. Order: [0] route, [1] plan (all plan kernels and the gather),
+ * events. Order: [0] route (moe_route or moe_gate), [1] plan (all plan kernels and the gather),
  * [2] producer, [3] consumer, [4] scale, [5] gather only, and [6] the producer's
  * execution span on the device clock (its first CTA's start to its last CTA's end;
  * unlike [2] it excludes time spent queued behind other kernels, for example those

@@ -142,3 +142,4 @@ def test_plan_calls_reject_a_null_plan(lib):
     assert lib_.moe_set_schedule(None, 0, 1) == capi.MOE_ERR_ARG
     assert lib_.moe_launch_info(None, None, None, None, None) == capi.MOE_ERR_ARG
     assert lib_.moe_status(None, None, None, None) == capi.MOE_ERR_ARG
+    assert lib_.moe_gate(None, None, None, None, None, None, None, 0, None) == capi.MOE_ERR_ARG

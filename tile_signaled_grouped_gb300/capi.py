@@ -77,6 +77,7 @@ def load():
         "moe_plan_create": (ip, [P(moe_cfg), vp, sz, P(vp), sz, P(vp)]),
         "moe_plan_destroy": (None, [vp]),
         "moe_route": (ip, [vp, vp, vp, vp, vp, vp]),
+        "moe_gate": (ip, [vp, P(vp), vp, vp, vp, vp, vp, ip, vp]),
         "moe_plan_build": (ip, [vp, vp, P(vp), vp]),
         "moe_expert_combine": (ip, [vp, P(vp), P(vp), P(vp), P(vp), vp, vp]),
         "moe_scale": (ip, [vp, vp, P(vp), P(vp), vp]),
@@ -148,6 +149,11 @@ def moe_plan_destroy(plan: int):
 
 def moe_route(plan, logits, forced_ids, topk_ids, topk_w, stream):
     check(lib().moe_route(plan, logits, forced_ids, topk_ids, topk_w, stream), "moe_route")
+
+
+def moe_gate(plan, x, w_router, forced_ids, topk_ids, topk_w, logits, splits, stream):
+    check(lib().moe_gate(plan, ptr_array(x), w_router, forced_ids, topk_ids, topk_w, logits,
+                         splits, stream), "moe_gate")
 
 
 def moe_plan_build(plan, topk_ids, x, stream):

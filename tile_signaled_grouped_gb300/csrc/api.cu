@@ -33,6 +33,8 @@ struct moe_plan {
   int num_sms;
   int pair_clusters;        // CTA pairs of the pair producer resident at once (0: unknown)
   int pair_clusters_fused;  // the same for its fused variant
+  int gate_npad;            // gate MMA N (E rounded up to 32), 0 when E > kGateMaxE
+  int gate_clusters[4];     // gate clusters resident at once for splits 1, 2, 4, 8
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   cudaEvent_t ev_ready, ev_join;
   cudaEvent_t ev_t0[kTSlots][kTRing], ev_t1[kTSlots][kTRing];
@@ -273,7 +275,8 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
 
   if (preload_producer() != cudaSuccess || preload_producer_pair() != cudaSuccess ||
       preload_consumer() != cudaSuccess ||
-      preload_plan() != cudaSuccess || preload_route_scale() != cudaSuccess)
+      preload_plan() != cudaSuccess || preload_route_scale() != cudaSuccess ||
+      preload_gate() != cudaSuccess)
     return MOE_ERR_CUDA;
 
   void* fn = nullptr;
@@ -295,6 +298,9 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
   p->num_sms = prop.multiProcessorCount;
   p->pair_clusters = producer_pair_max_clusters(false);
   p->pair_clusters_fused = producer_pair_max_clusters(true);
+  p->gate_npad = d.E <= kGateMaxE ? (d.E + 31) / 32 * 32 : 0;
+  for (int i = 0; i < 4; ++i)
+    p->gate_clusters[i] = p->gate_npad > 0 ? gate_clusters(d.E, 1 << i) : 0;
   p->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   bool ok = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) == cudaSuccess;
@@ -330,6 +336,41 @@ int moe_route(moe_plan* p, const float* logits, const int32_t* forced, int32_t* 
   const DevPlan dp = dev_plan(p);
   tstart(p, kTRoute, s);
   CUDA_TRY(launch_route(dp, logits, forced, ids, w, s));
+  tstop(p, kTRoute, s);
+  return MOE_OK;
+}
+
+int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int32_t* forced,
+             int32_t* ids, float* w, float* logits, int splits, moe_stream_t stream) {
+  if (p == nullptr || x == nullptr || !aligned16(w_router) || ids == nullptr || w == nullptr)
+    return MOE_ERR_ARG;
+  if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8) return MOE_ERR_ARG;
+  const Dims& d = p->d;
+  const int lg = splits == 8 ? 3 : splits == 4 ? 2 : splits == 2 ? 1 : 0;
+  if (p->gate_npad == 0 || (splits != 0 && p->gate_clusters[lg] == 0)) return MOE_ERR_UNSUPPORTED;
+  GateArgs ga{};
+  ga.npad = p->gate_npad;
+  for (int r = 0; r < d.W; ++r)
+    if (!aligned16(x[r]) || !make_map(p, &ga.tm_x[r], x[r], d.T, d.D, kTileM)) return MOE_ERR_ARG;
+  if (!make_map(p, &ga.tm_r, w_router, d.E, d.D, (uint32_t)ga.npad)) return MOE_ERR_ARG;
+  ga.forced = forced;
+  ga.ids = ids;
+  ga.w = w;
+  ga.logits = logits;
+  ga.p = dev_plan(p);
+  if (splits == 0) {
+    // The largest split whose clusters all run at once (one wave: a second wave
+    // costs a whole tile's time) and that leaves every CTA at least four K blocks.
+    const int tiles = d.W * ((d.T + kTileM - 1) / kTileM);
+    const int nk = d.D / kBlockK;
+    splits = 1;
+    for (int i = 1; i < 4; ++i)
+      if (tiles <= p->gate_clusters[i] && nk >= (4 << i)) splits = 1 << i;
+  }
+  ga.splits = splits;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  tstart(p, kTRoute, s);
+  CUDA_TRY(launch_gate(ga, s));
   tstop(p, kTRoute, s);
   return MOE_OK;
 }

@@ -100,23 +100,6 @@ static_assert(PairCfg<false>::kSmem <= 227 * 1024, "pair producer shared memory"
 static_assert(PairCfg<true>::kSmem <= 227 * 1024, "fused pair producer shared memory");
 
 // --- cluster and cta_group::2 forms ------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address of the same shared variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_shared(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
                : "memory");

@@ -109,6 +109,25 @@ cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s);
 cudaError_t launch_gather(const DevPlan& p, const __nv_bfloat16* const* x,
                           __nv_bfloat16* const* xbuf, int num_sms, cudaStream_t s);
 
+// Gate: router GEMM (tcgen05) fused with softmax and top-k. E <= kGateMaxE.
+constexpr int kGateMaxE = 256;
+struct GateArgs {
+  CUtensorMap tm_x[MOE_MAX_RANKS];  // rank s's tokens [T][D], boxes of 128 rows
+  CUtensorMap tm_r;                 // router [E][D], boxes of npad rows
+  const int32_t* forced;            // [W][T][k] or null
+  int32_t* ids;                     // [W][T][k]
+  float* w;                         // [W][T][k]
+  float* logits;                    // [W][T][E] or null
+  DevPlan p;
+  int npad;    // MMA N: E rounded up to 32
+  int splits;  // CTAs of one cluster sharing a token tile, each summing a K range
+};
+cudaError_t preload_gate();
+// Clusters of `splits` CTAs (1, 2, 4 or 8) resident at once on an idle GPU, for E
+// experts (0: that split cannot be launched).
+int gate_clusters(int E, int splits);
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
+
 struct ProducerArgs {
   CUtensorMap tm_x[MOE_MAX_RANKS];
   CUtensorMap tm_h[MOE_MAX_RANKS];
@@ -292,6 +311,36 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// --- thread-block clusters ------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_shared(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes before the
+// barrier with reads of any CTA after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+// 16-byte load from the shared memory of a CTA of the cluster (cl_addr 16-byte aligned).
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t cl_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cl_addr)
+               : "memory");
+  return v;
 }
 
 // --- tcgen05 --------------------------------------------------------------

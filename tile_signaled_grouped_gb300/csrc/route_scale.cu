@@ -7,79 +7,31 @@
 #include <algorithm>
 
 #include "moe_common.cuh"
+#include "route_topk.cuh"
 
 namespace moe {
 namespace {
 
-// One warp per token: softmax over E logits (fp32), then k rounds of a warp
-// argmax on (logit descending, expert id ascending). Comparing logits decides
-// the same order as comparing probabilities, without rounding ties. Each lane
-// holds PER logits (E <= 32 * PER); the launcher picks the smallest PER.
+// One warp per token: its E logits (fp32) through route_group. Each lane holds PER
+// logits (E <= 32 * PER); the launcher picks the smallest PER.
 template <int PER>
 __global__ void __launch_bounds__(256) route_kernel(DevPlan p, const float* __restrict__ logits,
                                                     const int32_t* __restrict__ forced,
                                                     int32_t* __restrict__ ids,
                                                     float* __restrict__ w) {
-  constexpr int kMaxPerLane = PER;
   const Dims d = p.d;
   const int lane = threadIdx.x & 31;
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (tok >= d.W * d.T) return;
   const float* lg = logits + (size_t)tok * d.E;
-  float v[kMaxPerLane];
-  float mx = -INFINITY;
+  float v[PER];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
     v[i] = e < d.E ? lg[e] : -INFINITY;
-    mx = fmaxf(mx, v[i]);
   }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i)
-    if (lane + 32 * i < d.E) sum += expf(v[i] - mx);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float inv = 1.0f / sum;
-
-  if (forced != nullptr) {
-    for (int j = lane; j < d.k; j += 32) {
-      const int e = forced[(size_t)tok * d.k + j];
-      ids[(size_t)tok * d.k + j] = e;
-      w[(size_t)tok * d.k + j] = (e >= 0 && e < d.E) ? expf(lg[e] - mx) * inv : 0.f;
-    }
-    return;
-  }
-  uint32_t taken = 0;  // bit i: this lane's candidate i already chosen
-  for (int j = 0; j < d.k; ++j) {
-    float bv = -INFINITY;
-    int be = INT_MAX, bi = -1;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < d.E && !(taken >> i & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
-        bi = i;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if (bi >= 0 && lane + 32 * bi == be) taken |= 1u << bi;
-    if (lane == 0) {
-      ids[(size_t)tok * d.k + j] = be;
-      w[(size_t)tok * d.k + j] = expf(bv - mx) * inv;
-    }
-  }
+  route_group<32, PER>(v, d.E, d.k, forced != nullptr ? forced + (size_t)tok * d.k : nullptr,
+                       ids + (size_t)tok * d.k, w + (size_t)tok * d.k, lane);
 }
 
 // One warp per token (s, t): out_s[t] = sum_j w_j * row_j, fp32 in slot order.

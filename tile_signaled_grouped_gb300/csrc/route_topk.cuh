@@ -1,0 +1,153 @@
+// Routing of one token by a warp or by one thread: softmax over its E gate scores
+// and the top k.
+//
+// TileMoE notes (zhongzhuzhou.org), section 2.1 and 2.2 step 1: the router turns a
+// token's scores into a probability distribution over the E experts and keeps the
+// k most probable ones; the gate weights are those probabilities (not renormalised
+// over the k). Used by the routing kernel (a warp per token, scores read from
+// memory) and by the gate kernel (scores summed from its K-split partials).
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+#if defined(__CUDACC__)
+
+// Order-preserving map of a float to an unsigned key (larger float, larger key);
+// -0 is taken as +0, so equal values have equal keys.
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Compare-exchange of two (score, expert) candidates: afterwards slot i holds the
+// one that comes first (larger score, then lower id).
+template <int PER>
+__device__ __forceinline__ void route_cswap(float (&v)[PER], int (&e)[PER], int i, int j) {
+  const bool sw = (v[j] > v[i]) | ((v[j] == v[i]) & (e[j] < e[i]));
+  const float vi = v[i], vj = v[j];
+  const int ei = e[i], ej = e[j];
+  v[i] = sw ? vj : vi;
+  v[j] = sw ? vi : vj;
+  e[i] = sw ? ej : ei;
+  e[j] = sw ? ei : ej;
+}
+
+// One token, routed by G = 32 lanes (a whole warp, converged) or by G = 1 thread.
+// Lane lig of the group holds the scores of experts lig, lig + G, ... (PER of them;
+// -inf past E). Writes ids_row[0..k) and w_row[0..k) (from lig == 0). The decision
+// compares scores, larger first, equal scores to the lower expert id: the order of
+// the probabilities without their rounding ties. With forced_row, the ids are
+// those and the weights the probabilities at them (0 for an id out of range, which
+// the plan build reports).
+//
+// Cost. Every step is branch-free: padded candidates hold -inf, so exp adds an
+// exact 0 for them and they never win. A warp's reductions are redux.sync over all
+// 32 lanes (one instruction each; a reduction over part of a warp runs once per
+// distinct lane mask, so groups of 2 to 16 lanes would be slower). With PER <= 8 a
+// lane sorts its candidates once (odd-even transposition) and each of the k rounds
+// is two reductions and a shift of the winner's list; with more candidates per lane
+// each round rescans them (the first strict maximum in ascending id order).
+template <int G, int PER>
+__device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int k,
+                                            const int32_t* forced_row, int32_t* ids_row,
+                                            float* w_row, int lig) {
+  static_assert(G == 1 || G == 32, "a thread or a whole warp per token");
+  static_assert(PER <= 32, "candidates per lane");
+  constexpr uint32_t kAll = 0xFFFFFFFFu;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) mx = fmaxf(mx, vin[i]);
+  if (G > 1) mx = key_float(__reduce_max_sync(kAll, float_key(mx)));
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) sum += expf(vin[i] - mx);
+#pragma unroll
+  for (int o = G / 2; o; o >>= 1) sum += __shfl_xor_sync(kAll, sum, o);
+  const float inv = 1.0f / sum;
+
+  if (forced_row != nullptr) {
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(forced_row + j);
+      const bool in = e >= 0 && e < E;
+      float ve = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) ve = (in && e == lig + G * i) ? vin[i] : ve;
+      if (G > 1) ve = __shfl_sync(kAll, ve, in ? e % G : 0);
+      const float wj = in ? expf(ve - mx) * inv : 0.f;
+      if (lig == 0) {
+        ids_row[j] = e;
+        w_row[j] = wj;
+      }
+    }
+    return;
+  }
+  if (PER <= 8) {
+    float v[PER];
+    int e[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      v[i] = vin[i];
+      e[i] = lig + G * i;
+    }
+#pragma unroll
+    for (int r = 0; r < PER; ++r)
+#pragma unroll
+      for (int i = r & 1; i + 1 < PER; i += 2) route_cswap<PER>(v, e, i, i + 1);
+    for (int j = 0; j < k; ++j) {
+      // The group's best head: the largest key, then the lowest id holding it.
+      const uint32_t key = float_key(v[0]);
+      const uint32_t kmax = G > 1 ? __reduce_max_sync(kAll, key) : key;
+      const uint32_t cand = key == kmax ? (uint32_t)e[0] : 0xFFFFFFFFu;
+      const uint32_t emin = G > 1 ? __reduce_min_sync(kAll, cand) : cand;
+      const bool win = (uint32_t)e[0] == emin;
+#pragma unroll
+      for (int i = 0; i + 1 < PER; ++i) {
+        v[i] = win ? v[i + 1] : v[i];
+        e[i] = win ? e[i + 1] : e[i];
+      }
+      v[PER - 1] = win ? -INFINITY : v[PER - 1];
+      e[PER - 1] = win ? 0x7FFFFFFF : e[PER - 1];
+      const float wj = expf(key_float(kmax) - mx) * inv;
+      if (lig == 0) {
+        ids_row[j] = (int32_t)emin;
+        w_row[j] = wj;
+      }
+    }
+  } else {
+    uint32_t taken = 0;  // bit i: this lane's candidate i already chosen
+    for (int j = 0; j < k; ++j) {
+      // This lane's best candidate not yet taken: the first strict maximum in
+      // ascending id order, so equal scores keep the lower id (a score of -inf
+      // still counts once nothing else is left).
+      float bv = -INFINITY;
+      int bi = -1;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const bool better = !((taken >> i) & 1u) & (lig + G * i < E) & ((vin[i] > bv) | (bi < 0));
+        bv = better ? vin[i] : bv;
+        bi = better ? i : bi;
+      }
+      const uint32_t be = bi >= 0 ? (uint32_t)(lig + G * bi) : 0xFFFFFFFFu;
+      const uint32_t key = float_key(bv);
+      const uint32_t kmax = G > 1 ? __reduce_max_sync(kAll, key) : key;
+      const uint32_t cand = key == kmax ? be : 0xFFFFFFFFu;
+      const uint32_t emin = G > 1 ? __reduce_min_sync(kAll, cand) : cand;
+      taken |= (bi >= 0 && be == emin) ? 1u << bi : 0u;
+      const float wj = expf(key_float(kmax) - mx) * inv;
+      if (lig == 0) {
+        ids_row[j] = (int32_t)emin;
+        w_row[j] = wj;
+      }
+    }
+  }
+}
+
+#endif  // __CUDACC__
+
+}  // namespace moe

@@ -67,6 +67,19 @@ class ExpertCombine:
                        self.ids.data_ptr(), self.w.data_ptr(), _stream_handle(stream))
         return self.ids, self.w
 
+    def gate(self, x, w_router, forced_ids=None, stream=None, logits_out=None, splits=0):
+        """Router scores of the token rows and their routing, in one kernel.
+
+        x: W tensors [T, D] bf16; w_router: [E, D] bf16 (E <= 256). logits_out: an
+        optional [W, T, E] fp32 tensor that receives the scores. splits: 0 picks the
+        K split, else 1, 2, 4 or 8."""
+        capi.moe_gate(self.plan, [t.data_ptr() for t in x], w_router.data_ptr(),
+                      None if forced_ids is None else forced_ids.data_ptr(),
+                      self.ids.data_ptr(), self.w.data_ptr(),
+                      None if logits_out is None else logits_out.data_ptr(), splits,
+                      _stream_handle(stream))
+        return self.ids, self.w
+
     def plan_build(self, x, ids=None, stream=None):
         ids = self.ids if ids is None else ids
         capi.moe_plan_build(self.plan, ids.data_ptr(), [t.data_ptr() for t in x],
@@ -87,19 +100,26 @@ class ExpertCombine:
                        [t.data_ptr() for t in out], _stream_handle(stream))
         return out
 
-    def forward(self, x, w_gate, w_up, w_down, logits, forced_ids=None, producer=None,
-                consumer=None, out=None):
+    def forward(self, x, w_gate, w_up, w_down, logits=None, forced_ids=None, producer=None,
+                consumer=None, out=None, w_router=None):
         """route -> plan -> overlapped FFN and combine -> scale; all on the GPU.
 
-        Every call is enqueued on `producer` (and `consumer`): inputs written on
-        another stream must be complete before it (an event or a synchronize)."""
-        self.route(logits, forced_ids, producer)
+        The routing comes from the gate logits, or, given w_router instead, from the
+        router's scores of x (gate()). Every call is enqueued on `producer` (and
+        `consumer`): inputs written on another stream must be complete before it (an
+        event or a synchronize)."""
+        if (logits is None) == (w_router is None):
+            raise ValueError("give exactly one of logits and w_router")
+        if w_router is not None:
+            self.gate(x, w_router, forced_ids, producer)
+        else:
+            self.route(logits, forced_ids, producer)
         self.plan_build(x, stream=producer)
         self.expert_combine(w_gate, w_up, w_down, producer, consumer)
         return self.scale(stream=producer, out=out)
 
-    def capture(self, x, w_gate, w_up, w_down, logits, forced_ids=None, producer=None,
-                consumer=None, out=None):
+    def capture(self, x, w_gate, w_up, w_down, logits=None, forced_ids=None, producer=None,
+                consumer=None, out=None, w_router=None):
         """Records one step (route, plan, combine, scale) into a CUDA graph over these
         tensors. Replaying it (graph.replay()) runs the step on whatever the tensors hold
         then, with one launch from the host. Every call the step makes is asynchronous
@@ -111,7 +131,8 @@ class ExpertCombine:
         torch.cuda.synchronize(self.device)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=sp):
-            self.forward(x, w_gate, w_up, w_down, logits, forced_ids, sp, sc, out=out)
+            self.forward(x, w_gate, w_up, w_down, logits, forced_ids, sp, sc, out=out,
+                         w_router=w_router)
         return graph
 
     # ------------------------------------------------------------- inspection
@@ -177,7 +198,7 @@ class ExpertCombine:
         capi.moe_set_timing(self.plan, enable)
 
     def timings(self):
-        """[route, plan, producer, consumer, scale, gather, producer span] in ms (-1: none)."""
+        """[route or gate, plan, producer, consumer, scale, gather, producer span] in ms (-1: none)."""
         return capi.moe_timings(self.plan, 7)
 
 

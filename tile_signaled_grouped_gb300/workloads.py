@@ -19,7 +19,7 @@ import dataclasses
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "get_workload", "Inputs", "make_inputs"]
+__all__ = ["Workload", "WORKLOADS", "get_workload", "Inputs", "make_inputs", "router_weights"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -133,3 +133,10 @@ def make_inputs(wl: Workload, device="cpu", with_weights: bool = True) -> Inputs
     else:
         raise ValueError(f"unknown routing {wl.routing!r}")
     return Inputs(wl, x, w_gate, w_up, w_down, logits, forced)
+
+
+def router_weights(wl: Workload, device="cpu") -> torch.Tensor:
+    """Router weights [E, D] bf16 ~ N(0, 1/(D * x_std^2)): the scores of N(0, x_std)
+    token rows then have unit variance, like the drawn gate logits."""
+    std = 1.0 / (wl.d_model ** 0.5 * wl.x_std)
+    return _normal_bf16((wl.E, wl.d_model), std, device, wl.seed * 1000 + 3)
