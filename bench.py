@@ -352,6 +352,36 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     torch.cuda.synchronize()
     graph_ms = ev0.elapsed_time(ev1) / (iters * 4)
     del graph
+    # The gate kernel (router scores + softmax + top-k in one launch) on this shape's
+    # tokens with seeded router weights, L2 flushed before each launch. It is not
+    # part of the step (the workload's routing comes from its gate logits).
+    gate = {}
+    if wl.E <= 256:
+        from tile_signaled_grouped_gb300.workloads import router_weights
+        wr = router_weights(wl, device="cuda")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        lay2.set_timing(False)
+        for _ in range(3):
+            lay2.gate(inp.x, wr, stream=sp)
+        torch.cuda.synchronize()
+        g = []
+        for _ in range(iters):
+            with torch.cuda.stream(sp):
+                flush.zero_()
+            lay2.set_timing(True)
+            lay2.gate(inp.x, wr, stream=sp)
+            g.append(lay2.timings()[0])
+            lay2.set_timing(False)
+        gate_ms = statistics.median(g)
+        gate_bytes = 2.0 * D * W * T + 2.0 * D * wl.E + 8.0 * W * T * k
+        gate_flops = 2.0 * W * T * D * wl.E
+        gate = {"ms": gate_ms, "bytes": gate_bytes,
+                "gbs": gate_bytes / (gate_ms * 1e-3) / 1e9,
+                "frac_hbm": gate_bytes / (gate_ms * 1e-3) / 1e9 / hbm,
+                "tflops": gate_flops / (gate_ms * 1e-3) / 1e12,
+                "timing": "CUDA events around the launch (launch latency included), "
+                          "L2 flushed before each, median of %d" % iters}
+        del flush
     rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
     recv_rows = layer.field(capi.MOE_PLAN_RECV_ROWS).cpu().tolist()
     rows = sum(rank_rows)
@@ -376,6 +406,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         "scale_frac": scale_bytes / (over["scale"] * 1e-3) / 1e9 / hbm,
         "gather_gbs": gather_bytes / (over["gather"] * 1e-3) / 1e9,
         "gather_frac": gather_bytes / (over["gather"] * 1e-3) / 1e9 / hbm,
+        "gate": gate,
     }
 
 
