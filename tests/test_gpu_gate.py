@@ -122,6 +122,9 @@ GATE_SHAPES = [
     # k = E: every expert, ordered
     Workload("k_equals_E", W=2, L=2, topk=4, T=40, d_model=128, d_ff=128, tb_M=64,
              routing="gate"),
+    # E = 24 (a thread per token, 32 candidates), D of 10 K blocks: uneven K ranges
+    Workload("E24_T200", W=4, L=6, topk=3, T=200, d_model=640, d_ff=128, tb_M=64,
+             routing="gate"),
 ]
 
 
@@ -221,4 +224,35 @@ def test_forward_from_the_router(mode):
     tol = float(np.expm1(2 * bound.max()) + 2 * U * (base.E + 16))
     P.check_plan(layer, base, plan, ids, w, w_rtol=tol)
     P.check_layout_and_outputs(layer, base, inp, plan, ids, w)
+    layer.close()
+
+
+def test_captured_step_from_the_router_replays_bit_exactly():
+    """A whole step routed by the gate kernel, captured into a CUDA graph: replaying it
+    gives the eager step's outputs bit for bit (every kernel of the step, the gate's
+    K-split sum included, adds in a fixed order)."""
+    base = Workload("gate_graph", W=4, L=8, topk=4, T=160, d_model=512, d_ff=256, tb_M=64,
+                    routing="gate")
+    inp = P.inputs_for(base)
+    wr = router_weights(base, device="cuda")
+    layer = ExpertCombine(base.W, base.L, base.topk, base.T, base.d_model, base.d_ff,
+                          base.tb_M, base.mgb)
+    sp, sc = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    torch.cuda.synchronize()
+    layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, w_router=wr, producer=sp,
+                  consumer=sc)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    eager = [t.clone() for t in layer.out]
+    ids = layer.ids.clone()
+    for t in layer.out:
+        t.zero_()
+    graph = layer.capture(inp.x, inp.w_gate, inp.w_up, inp.w_down, w_router=wr, producer=sp,
+                          consumer=sc)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    assert torch.equal(layer.ids, ids)
+    assert all(torch.equal(a, b) for a, b in zip(eager, layer.out))
+    del graph
     layer.close()
