@@ -22,8 +22,9 @@
  * Conventions
  *  - All pointers are device pointers unless stated. The caller owns all
  *    memory; the library never allocates device memory and owns no stream.
- *  - Tensors are dense, row-major, bf16 unless stated; base pointers must be
- *    16-byte aligned. d_model and d_ff must be multiples of 128.
+ *  - Tensors are dense, row-major, bf16 unless stated; every tensor's base
+ *    pointer (bf16, int32 and fp32 alike) must be 16-byte aligned, or the call
+ *    returns MOE_ERR_ARG. d_model and d_ff must be multiples of 128.
  *  - Return value 0 (MOE_OK) or a negative MOE_ERR_* for errors detected on
  *    the host before anything is enqueued. Errors detected on the device
  *    (bad routing ids, a device wait that ran out of time) are sticky in the

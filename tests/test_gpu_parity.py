@@ -147,6 +147,14 @@ def test_host_argument_errors():
     plan = capi.moe_plan_create(cfg, plan_ws.data_ptr(), pb, ptrs, rb)
     with pytest.raises(capi.MoeError, match="ARG"):
         capi.moe_plan_build(plan, 0, [0] * wl.W, 0)
+    # Base pointers of int32 and fp32 arrays must be 16-byte aligned too (checked on the host).
+    ids = torch.zeros(wl.W * wl.T * wl.topk + 4, dtype=torch.int32, device="cuda")
+    x = [torch.zeros(wl.T, wl.d_model, dtype=torch.bfloat16, device="cuda") for _ in range(wl.W)]
+    with pytest.raises(capi.MoeError, match="ARG"):
+        capi.moe_plan_build(plan, ids.data_ptr() + 4, [t.data_ptr() for t in x], 0)
+    w = torch.zeros(wl.W * wl.T * wl.topk + 4, dtype=torch.float32, device="cuda")
+    with pytest.raises(capi.MoeError, match="ARG"):
+        capi.moe_route(plan, w.data_ptr(), None, ids.data_ptr(), w.data_ptr() + 8, 0)
     capi.moe_plan_destroy(plan)
 
 

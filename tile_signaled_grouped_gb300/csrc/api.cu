@@ -185,6 +185,8 @@ LaunchShape launch_shape(const moe_plan* p, bool serial) {
 }
 
 bool aligned16(const void* ptr) { return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+// An optional pointer: null, or 16-byte aligned.
+bool null_or_aligned16(const void* ptr) { return ptr == nullptr || aligned16(ptr); }
 
 void tstart(moe_plan* p, int slot, cudaStream_t s) {
   if (p->timing) cudaEventRecord(p->ev_t0[slot][p->nrec[slot] % kTRing], s);
@@ -331,7 +333,9 @@ void moe_plan_destroy(moe_plan* p) {
 
 int moe_route(moe_plan* p, const float* logits, const int32_t* forced, int32_t* ids, float* w,
               moe_stream_t stream) {
-  if (p == nullptr || !aligned16(logits) || ids == nullptr || w == nullptr) return MOE_ERR_ARG;
+  if (p == nullptr || !aligned16(logits) || !null_or_aligned16(forced) || !aligned16(ids) ||
+      !aligned16(w))
+    return MOE_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const DevPlan dp = dev_plan(p);
   tstart(p, kTRoute, s);
@@ -342,7 +346,8 @@ int moe_route(moe_plan* p, const float* logits, const int32_t* forced, int32_t* 
 
 int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int32_t* forced,
              int32_t* ids, float* w, float* logits, int splits, moe_stream_t stream) {
-  if (p == nullptr || x == nullptr || !aligned16(w_router) || ids == nullptr || w == nullptr)
+  if (p == nullptr || x == nullptr || !aligned16(w_router) || !null_or_aligned16(forced) ||
+      !aligned16(ids) || !aligned16(w) || !null_or_aligned16(logits))
     return MOE_ERR_ARG;
   if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8) return MOE_ERR_ARG;
   const Dims& d = p->d;
@@ -376,7 +381,7 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
 }
 
 int moe_plan_build(moe_plan* p, const int32_t* ids, const void* const* x, moe_stream_t stream) {
-  if (p == nullptr || ids == nullptr || x == nullptr) return MOE_ERR_ARG;
+  if (p == nullptr || !aligned16(ids) || x == nullptr) return MOE_ERR_ARG;
   for (int r = 0; r < p->d.W; ++r)
     if (!aligned16(x[r])) return MOE_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -490,7 +495,7 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
 
 int moe_scale(moe_plan* p, const float* topk_w, const void* const* recv, void* const* out,
               moe_stream_t stream) {
-  if (p == nullptr || topk_w == nullptr || recv == nullptr || out == nullptr) return MOE_ERR_ARG;
+  if (p == nullptr || !aligned16(topk_w) || recv == nullptr || out == nullptr) return MOE_ERR_ARG;
   const Dims& d = p->d;
   ScaleArgs a;
   std::memset(&a, 0, sizeof(a));

@@ -45,8 +45,8 @@ extern "C" int moe_plan_build_noalloc(const moe_cfg* cfg, const int32_t* topk_id
   Dims d;
   const int rc = dims_from_cfg(cfg, &d);
   if (rc != MOE_OK) return rc;
-  if (topk_ids == nullptr || plan_out == nullptr ||
-      (reinterpret_cast<uintptr_t>(plan_out) & 255) != 0)
+  if (topk_ids == nullptr || (reinterpret_cast<uintptr_t>(topk_ids) & 15) != 0 ||
+      plan_out == nullptr || (reinterpret_cast<uintptr_t>(plan_out) & 255) != 0)
     return MOE_ERR_ARG;
   size_t off[PA_COUNT], cnt[PA_COUNT];
   if (plan_out_bytes < plan_layout(d, off, cnt)) return MOE_ERR_WORKSPACE;
