@@ -54,6 +54,48 @@ def test_pipelined_steps_equal_plain_forward(name, n_layers, cctas):
             assert torch.equal(got, ref), f"step with input set {i}"
 
 
+@pytest.mark.parametrize("n_layers", [1, 2])
+def test_pipelined_steps_routed_by_the_gate(n_layers):
+    """The same with the routing taken by the gate kernel from the copied tokens (no
+    logits cross the host link): every step equals a plain forward with the router."""
+    from tile_signaled_grouped_gb300.workloads import router_weights
+
+    name = "tiny"
+    base = get_workload(name)
+    sets = [make_inputs(get_workload(name, seed=s), device="cuda", with_weights=s == 0)
+            for s in (0, 3, 5)]
+    w = sets[0]
+    wr = router_weights(base, device="cuda")
+    torch.cuda.synchronize()
+    mk = lambda: ExpertCombine(base.W, base.L, base.topk, base.T, base.d_model, base.d_ff,
+                               base.tb_M, base.mgb)
+    ref_layer = mk()
+    sp, sc = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    want = []
+    for inp in sets:
+        out = ref_layer.forward(inp.x, w.w_gate, w.w_up, w.w_down, w_router=wr, producer=sp,
+                                consumer=sc)
+        torch.cuda.synchronize()
+        assert ref_layer.status() == (0, 0)
+        want.append([t.cpu().clone() for t in out])
+    layers = [mk() for _ in range(n_layers)]
+    pipe = HostPipeline(layers if n_layers > 1 else layers[0])
+    order = [0, 1, 2, 2, 0]
+    houts = []
+    for i in order:
+        hx = [t.cpu().pin_memory() for t in sets[i].x]
+        hout = [torch.empty(base.T, base.d_model, dtype=torch.bfloat16).pin_memory()
+                for _ in range(base.W)]
+        pipe.step(hx, None, None, hout, w.w_gate, w.w_up, w.w_down, w_router=wr)
+        houts.append(hout)
+    pipe.done_event().synchronize()
+    torch.cuda.synchronize()
+    assert all(lay.status() == (0, 0) for lay in layers)
+    for i, hout in zip(order, houts):
+        for got, ref in zip(hout, want[i]):
+            assert torch.equal(got, ref), f"step with input set {i}"
+
+
 def test_tuned_schedule_keeps_results_exact():
     """The adaptive schedule picks one of its candidates; the plan it then builds (new
     mgb) matches the oracle bit for bit, and the outputs the one-shot forward's."""

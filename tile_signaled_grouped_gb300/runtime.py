@@ -248,11 +248,16 @@ class HostPipeline:
     def sp0(self):
         return self.sp[0]
 
-    def step(self, hx, hlogits, hforced, hout, w_gate, w_up, w_down, start_after=None):
+    def step(self, hx, hlogits, hforced, hout, w_gate, w_up, w_down, start_after=None,
+             w_router=None):
         """Enqueue one step. hx: W pinned [T, D] bf16; hlogits: pinned [W, T, E] fp32;
         hforced: pinned [W, T, k] int32 or None; hout: W pinned [T, D] bf16 written when
         the step's output copy completes (after self.done_event() of this step).
-        start_after: an event the first copy must follow (for timing)."""
+        start_after: an event the first copy must follow (for timing). With w_router
+        (a device [E, D] bf16 tensor) the routing comes from the gate kernel on the
+        copied tokens and hlogits must be None: no logits cross the host link."""
+        if (hlogits is None) == (w_router is None):
+            raise ValueError("give exactly one of hlogits and w_router")
         b = self.i % self.nbuf
         li = self.i % len(self.layers)
         lay, sp, sc = self.layers[li], self.sp[li], self.sc[li]
@@ -263,12 +268,17 @@ class HostPipeline:
         with torch.cuda.stream(self.s_in):
             for d, h in zip(self.x[b], hx):
                 d.copy_(h, non_blocking=True)
-            self.logits[b].copy_(hlogits, non_blocking=True)
+            if hlogits is not None:
+                self.logits[b].copy_(hlogits, non_blocking=True)
             if hforced is not None:
                 self.forced[b].copy_(hforced, non_blocking=True)
         self.ev_in[b].record(self.s_in)
         sp.wait_event(self.ev_in[b])
-        lay.route(self.logits[b], self.forced[b] if hforced is not None else None, sp)
+        fid = self.forced[b] if hforced is not None else None
+        if w_router is not None:
+            lay.gate(self.x[b], w_router, fid, sp)
+        else:
+            lay.route(self.logits[b], fid, sp)
         lay.plan_build(self.x[b], stream=sp)
         self.ev_free[b].record(sp)
         lay.expert_combine(w_gate, w_up, w_down, sp, sc)
