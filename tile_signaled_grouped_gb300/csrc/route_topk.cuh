@@ -38,6 +38,31 @@ __device__ __forceinline__ void route_cswap(float (&v)[PER], int (&e)[PER], int 
   e[j] = sw ? ei : ej;
 }
 
+// Sorts a lane's candidates, first one first: Batcher's odd-even merge networks for
+// 2, 4 and 8 inputs (1, 5 and 19 compare-exchanges; every key (score, id) is
+// distinct, so any sorting network gives the same order).
+template <int PER>
+__device__ __forceinline__ void route_sort(float (&v)[PER], int (&e)[PER]) {
+  if constexpr (PER == 2) {
+    route_cswap<PER>(v, e, 0, 1);
+  } else if constexpr (PER == 4) {
+    constexpr int kNet[5][2] = {{0, 1}, {2, 3}, {0, 2}, {1, 3}, {1, 2}};
+#pragma unroll
+    for (int c = 0; c < 5; ++c) route_cswap<PER>(v, e, kNet[c][0], kNet[c][1]);
+  } else if constexpr (PER == 8) {
+    constexpr int kNet[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                                 {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                                 {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+    for (int c = 0; c < 19; ++c) route_cswap<PER>(v, e, kNet[c][0], kNet[c][1]);
+  } else {
+#pragma unroll
+    for (int r = 0; r < PER; ++r)
+#pragma unroll
+      for (int i = r & 1; i + 1 < PER; i += 2) route_cswap<PER>(v, e, i, i + 1);
+  }
+}
+
 // One token, routed by G = 32 lanes (a whole warp, converged) or by G = 1 thread.
 // Lane lig of the group holds the scores of experts lig, lig + G, ... (PER of them;
 // -inf past E). Writes ids_row[0..k) and w_row[0..k) (from lig == 0). The decision
@@ -50,9 +75,11 @@ __device__ __forceinline__ void route_cswap(float (&v)[PER], int (&e)[PER], int 
 // exact 0 for them and they never win. A warp's reductions are redux.sync over all
 // 32 lanes (one instruction each; a reduction over part of a warp runs once per
 // distinct lane mask, so groups of 2 to 16 lanes would be slower). With PER <= 8 a
-// lane sorts its candidates once (odd-even transposition) and each of the k rounds
-// is two reductions and a shift of the winner's list; with more candidates per lane
-// each round rescans them (the first strict maximum in ascending id order).
+// lane sorts its candidates once (route_sort) and each of the k rounds is two
+// reductions and a shift of the winner's list; with more candidates per lane each
+// round rescans them (the first strict maximum in ascending id order). A warp keeps
+// round j's winner in lane j and computes the k weights after the rounds, one exp
+// per lane, so no exp sits on the rounds' chain of reductions.
 template <int G, int PER>
 __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int k,
                                             const int32_t* forced_row, int32_t* ids_row,
@@ -95,10 +122,8 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
       v[i] = vin[i];
       e[i] = lig + G * i;
     }
-#pragma unroll
-    for (int r = 0; r < PER; ++r)
-#pragma unroll
-      for (int i = r & 1; i + 1 < PER; i += 2) route_cswap<PER>(v, e, i, i + 1);
+    route_sort<PER>(v, e);
+    uint32_t my_key = 0, my_id = 0;  // G = 32: round lig's winner
     for (int j = 0; j < k; ++j) {
       // The group's best head: the largest key, then the lowest id holding it.
       const uint32_t key = float_key(v[0]);
@@ -113,14 +138,21 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
       }
       v[PER - 1] = win ? -INFINITY : v[PER - 1];
       e[PER - 1] = win ? 0x7FFFFFFF : e[PER - 1];
-      const float wj = expf(key_float(kmax) - mx) * inv;
-      if (lig == 0) {
+      if (G > 1) {
+        my_key = lig == j ? kmax : my_key;
+        my_id = lig == j ? emin : my_id;
+      } else {
         ids_row[j] = (int32_t)emin;
-        w_row[j] = wj;
+        w_row[j] = expf(key_float(kmax) - mx) * inv;
       }
+    }
+    if (G > 1 && lig < k) {
+      ids_row[lig] = (int32_t)my_id;
+      w_row[lig] = expf(key_float(my_key) - mx) * inv;
     }
   } else {
     uint32_t taken = 0;  // bit i: this lane's candidate i already chosen
+    uint32_t my_key = 0, my_id = 0;  // G = 32: round lig's winner
     for (int j = 0; j < k; ++j) {
       // This lane's best candidate not yet taken: the first strict maximum in
       // ascending id order, so equal scores keep the lower id (a score of -inf
@@ -129,7 +161,8 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
       int bi = -1;
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
-        const bool better = !((taken >> i) & 1u) & (lig + G * i < E) & ((vin[i] > bv) | (bi < 0));
+        const bool better =
+            !((taken >> i) & 1u) & (lig + G * i < E) & ((vin[i] > bv) | (bi < 0));
         bv = better ? vin[i] : bv;
         bi = better ? i : bi;
       }
@@ -139,11 +172,17 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
       const uint32_t cand = key == kmax ? be : 0xFFFFFFFFu;
       const uint32_t emin = G > 1 ? __reduce_min_sync(kAll, cand) : cand;
       taken |= (bi >= 0 && be == emin) ? 1u << bi : 0u;
-      const float wj = expf(key_float(kmax) - mx) * inv;
-      if (lig == 0) {
+      if (G > 1) {
+        my_key = lig == j ? kmax : my_key;
+        my_id = lig == j ? emin : my_id;
+      } else {
         ids_row[j] = (int32_t)emin;
-        w_row[j] = wj;
+        w_row[j] = expf(key_float(kmax) - mx) * inv;
       }
+    }
+    if (G > 1 && lig < k) {
+      ids_row[lig] = (int32_t)my_id;
+      w_row[lig] = expf(key_float(my_key) - mx) * inv;
     }
   }
 }
