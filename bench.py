@@ -289,6 +289,89 @@ def gpu_arm(args, rank, world, local_rank):
     return result
 
 
+def measure_gate(lay, x, wl, stream, iters, warmup, hbm):
+    """The gate kernel (router scores + softmax + top-k in one launch) on the tokens x
+    with the workload's seeded router, L2 flushed before each launch; CUDA events of
+    the library around each launch (launch latency included), median."""
+    import torch
+
+    from tile_signaled_grouped_gb300.workloads import router_weights
+
+    W, T, D, k = wl.W, wl.T, wl.d_model, wl.topk
+    wr = router_weights(wl, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    lay.set_timing(False)
+    for _ in range(warmup):
+        lay.gate(x, wr, stream=stream)
+    torch.cuda.synchronize()
+    g = []
+    for _ in range(iters):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        lay.set_timing(True)
+        lay.gate(x, wr, stream=stream)
+        g.append(lay.timings()[0])
+        lay.set_timing(False)
+    code, detail = lay.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail} in the gate kernel")
+    ms = statistics.median(g)
+    nbytes = 2.0 * D * W * T + 2.0 * D * wl.E + 8.0 * W * T * k
+    flops = 2.0 * W * T * D * wl.E
+    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+            "tflops": flops / (ms * 1e-3) / 1e12,
+            "timing": "CUDA events around the launch (launch latency included), "
+                      "L2 flushed before each, median of %d" % iters}
+
+
+def gate_arm(args):
+    """--gate-only: the gate kernel alone on the workload's tokens (its own routing,
+    seeded router, no expert weights allocated), one JSON line."""
+    import dataclasses
+
+    import torch
+
+    from tile_signaled_grouped_gb300.runtime import ExpertCombine
+    from tile_signaled_grouped_gb300.workloads import get_workload, make_inputs
+
+    wl = get_workload(args.workload, routing="gate")
+    if args.tokens_per_rank:
+        wl = dataclasses.replace(wl, T=args.tokens_per_rank)
+    if wl.E > 256:
+        raise SystemExit(f"the gate kernel takes E <= 256 experts ({wl.name} has {wl.E})")
+    torch.cuda.set_device(0)
+    inp = make_inputs(wl, device="cuda", with_weights=False)
+    torch.cuda.synchronize()
+    lay = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb)
+    sp = torch.cuda.Stream()
+    hbm, _, _, src = _peaks()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
+    except Exception:
+        gpu_id = "0"
+    with ClockSampler(gpu_id) as clk:
+        g = measure_gate(lay, inp.x, wl, sp, args.steps, args.warmup, hbm)
+    lay.close()
+    ntok = wl.W * wl.T
+    return {
+        "metric": "gate tokens/s", "value": ntok / (g["ms"] * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": g["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded: x~N(0,1), router~N(0,1/D))",
+        "config": {"workload": wl.name, "kernel": "gate_kernel", "W": wl.W,
+                   "experts": wl.E, "topk": wl.topk, "tokens_per_rank": wl.T,
+                   "d_model": wl.d_model, "l2": "flushed before each launch"},
+        "roofline": {"kernel": "gate_kernel", "bound": "hbm", "achieved": g["gbs"],
+                     "peak": hbm, "unit": "GB/s", "frac": g["frac_hbm"], "traffic": None,
+                     "peak_source": f"{src} HBM copy", "bytes_per_launch": g["bytes"],
+                     "launch_ms": g["ms"], "launch_ms_source": g["timing"]},
+        "tflops": g["tflops"],
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+
+
 def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     """Per-kernel times of one step, and the producer alone on every SM (serial mode)."""
     import torch
@@ -355,33 +438,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     # The gate kernel (router scores + softmax + top-k in one launch) on this shape's
     # tokens with seeded router weights, L2 flushed before each launch. It is not
     # part of the step (the workload's routing comes from its gate logits).
-    gate = {}
-    if wl.E <= 256:
-        from tile_signaled_grouped_gb300.workloads import router_weights
-        wr = router_weights(wl, device="cuda")
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-        lay2.set_timing(False)
-        for _ in range(3):
-            lay2.gate(inp.x, wr, stream=sp)
-        torch.cuda.synchronize()
-        g = []
-        for _ in range(iters):
-            with torch.cuda.stream(sp):
-                flush.zero_()
-            lay2.set_timing(True)
-            lay2.gate(inp.x, wr, stream=sp)
-            g.append(lay2.timings()[0])
-            lay2.set_timing(False)
-        gate_ms = statistics.median(g)
-        gate_bytes = 2.0 * D * W * T + 2.0 * D * wl.E + 8.0 * W * T * k
-        gate_flops = 2.0 * W * T * D * wl.E
-        gate = {"ms": gate_ms, "bytes": gate_bytes,
-                "gbs": gate_bytes / (gate_ms * 1e-3) / 1e9,
-                "frac_hbm": gate_bytes / (gate_ms * 1e-3) / 1e9 / hbm,
-                "tflops": gate_flops / (gate_ms * 1e-3) / 1e12,
-                "timing": "CUDA events around the launch (launch latency included), "
-                          "L2 flushed before each, median of %d" % iters}
-        del flush
+    gate = measure_gate(lay2, inp.x, wl, sp, iters, 3, hbm) if wl.E <= 256 else {}
     rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
     recv_rows = layer.field(capi.MOE_PLAN_RECV_ROWS).cpu().tolist()
     rows = sum(rank_rows)
@@ -536,6 +593,9 @@ def main():
                          "one batch's routing, plan and gather overlap the previous batch's FFN")
     ap.add_argument("--producer-pairs", type=int, default=1, choices=[0, 1],
                     help="1: the CTA-pair producer (clusters of two, tcgen05 cta_group::2)")
+    ap.add_argument("--gate-only", action="store_true",
+                    help="time the gate kernel alone (router scores + softmax + top-k) on the "
+                         "workload's tokens; one GPU")
     ap.add_argument("--ccta-sweep", type=lambda v: [int(x) for x in v.split(",") if x],
                     default=[-1, 0, 4, 8],
                     help="consumer-CTA counts whose step time is reported (outside the timed "
@@ -553,6 +613,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)), flush=True)
+        return
+    if args.gate_only:
+        if world > 1:
+            ap.error("--gate-only runs on one GPU")
+        print(json.dumps(gate_arm(args)), flush=True)
         return
 
     if world > 1:
