@@ -39,9 +39,11 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons. Only samples
+    stamped between mark_start() and mark_end() (host clock) are summarised: those the
+    sampler takes while the program is idle or warming up would read as full clocks."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -49,6 +51,15 @@ class ClockSampler:
         self.index = index  # physical index or "GPU-<uuid>"
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        import datetime
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        import datetime
+        self.t1 = datetime.datetime.now()
 
     def __enter__(self):
         try:
@@ -71,6 +82,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        import datetime
         if self.proc is None or self.file is None:
             return None
         self.file.flush()
@@ -78,18 +90,29 @@ class ClockSampler:
         with open(self.file.name) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) == 7:
-                    rows.append(parts)
+                if len(parts) == 8:
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    except ValueError:
+                        continue
+                    rows.append((ts, parts[1:]))
         os.unlink(self.file.name)
-        if not rows:
+        inside = [r for ts, r in rows
+                  if (self.t0 is None or ts >= self.t0) and (self.t1 is None or ts <= self.t1)]
+        window = "timed region"
+        if not inside:  # a region shorter than the sampling interval
+            inside, window = [r for _, r in rows], "whole sampler run (none inside the region)"
+        if not inside:
             return None
-        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        sm = [float(r[0]) for r in inside if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        pw = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "power_w_median": statistics.median(pw) if pw else None,
+                "samples": len(inside), "window": window}
 
 
 def producer_traffic(wl_name: str, tokens_override: int, pairs: int):
@@ -198,6 +221,7 @@ def gpu_arm(args, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+        clk.mark_start()
         t_wall = time.perf_counter()
         ev0.record(sp)
         for s_ in sps[1:]:
@@ -208,6 +232,7 @@ def gpu_arm(args, rank, world, local_rank):
             sp.wait_stream(s_)
         ev1.record(sp)
         torch.cuda.synchronize()
+        clk.mark_end()
         if world > 1:
             torch.distributed.barrier()
         wall = time.perf_counter() - t_wall
@@ -351,7 +376,9 @@ def gate_arm(args):
     except Exception:
         gpu_id = "0"
     with ClockSampler(gpu_id) as clk:
+        clk.mark_start()
         g = measure_gate(lay, inp.x, wl, sp, args.steps, args.warmup, hbm)
+        clk.mark_end()
     lay.close()
     ntok = wl.W * wl.T
     return {

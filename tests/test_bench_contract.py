@@ -79,3 +79,29 @@ def test_max_over_ranks_gloo_world2():
 
 def test_single_process_passthrough():
     assert bench.max_over_ranks(7.5) == 7.5
+
+
+def test_clock_summary_keeps_the_timed_region_only(tmp_path):
+    """Samples taken before the timed region (idle or warming up, full clocks) are left
+    out of the clock summary; throttle reasons come from the region's samples."""
+    import datetime
+
+    import bench
+
+    c = bench.ClockSampler(0)
+    path = tmp_path / "clocks.csv"
+    now = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    with open(path, "w") as f:
+        for i in range(10):
+            ts = (now + datetime.timedelta(milliseconds=100 * i)).strftime("%Y/%m/%d %H:%M:%S.%f")
+            busy = i >= 3
+            f.write(f"{ts[:-3]}, {1400 if busy else 2070}, 2070, 1300.5, Not Active, Not Active, "
+                    f"Not Active, {'Active' if busy else 'Not Active'}\n")
+    c.file = open(path)
+    c.proc = object()  # the sampler process has already ended
+    c.t0 = now + datetime.timedelta(milliseconds=250)
+    c.t1 = now + datetime.timedelta(milliseconds=950)
+    s = c.summary()
+    assert s["samples"] == 7 and s["window"] == "timed region"
+    assert s["sm_mhz"] == 1400 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
