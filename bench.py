@@ -106,12 +106,10 @@ class ClockSampler:
             return None
         sm = [float(r[0]) for r in inside if r[0].replace(".", "").isdigit()]
         mx = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
-        pw = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in inside for i in range(4) if r[3 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "power_w_median": statistics.median(pw) if pw else None,
                 "samples": len(inside), "window": window}
 
 
