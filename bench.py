@@ -247,6 +247,11 @@ def gpu_arm(args, rank, world, local_rank):
     e2e = e2e_arm(layers, inp, wl, sp, sc, args)
 
     # ---- stage measurements (outside the timed region) --------------------------------
+    # They time kernels one at a time against the burst peaks, so they start from a
+    # rested GPU: after the timed region and the e2e leg the power limiter holds the
+    # clocks down for a while, and a few idle seconds release it.
+    torch.cuda.synchronize()
+    time.sleep(3.0)
     stages = stage_times(layer, inp, wl, sp, sc, args)
 
     hbm, bf16, bf16_sus, src = _peaks()
