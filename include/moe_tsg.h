@@ -70,7 +70,8 @@ typedef struct moe_cfg {
   int L;             /* experts per rank (E = W*L, 1..1024) */
   int topk;          /* experts per token, 1..min(E, 32) */
   int T;             /* tokens per rank, >= 1 */
-  int d_model;       /* D, multiple of 128 */
+  int d_model;       /* D, multiple of 128, at most 10240 (a token row fits one 20 KB
+                        copy chunk; larger gives MOE_ERR_UNSUPPORTED) */
   int d_ff;          /* F, expert hidden size, multiple of 128 */
   int tb_M;          /* row-band height of the layout: 64, 128 or 256 */
   int mgb;           /* row bands merged into one middle segment (section 5.2), >= 1 */

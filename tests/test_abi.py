@@ -77,6 +77,13 @@ def test_invalid_configurations_are_rejected(lib, bad):
         capi.moe_workspace_size(_cfg(**bad))
 
 
+def test_token_rows_must_fit_one_copy_chunk(lib):
+    # The combine copy moves whole rows through 20 KB shared-memory slots.
+    assert capi.moe_workspace_size(_cfg(d_model=10240))[0] > 0
+    with pytest.raises(capi.MoeError, match="MOE_ERR_UNSUPPORTED"):
+        capi.moe_workspace_size(_cfg(d_model=10240 + 128))
+
+
 def test_cfg_struct_matches_the_header(lib):
     """The ctypes mirror of moe_cfg has the header's fields in the header's order."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)

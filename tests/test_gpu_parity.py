@@ -53,6 +53,15 @@ def test_small_shapes_full_parity(wl):
     _full_check(wl, "overlap", cctas=4)
 
 
+@pytest.mark.parametrize("mode", ["overlap", "fused"])
+def test_largest_token_row(mode):
+    """d_model = 10240, the largest the library takes: each copy chunk holds exactly one
+    20 KB row. Plan bit-exact, copies exact, outputs within tolerance."""
+    wl = Workload("D10240", W=2, L=2, topk=2, T=40, d_model=10240, d_ff=128, tb_M=64,
+                  routing="gate")
+    _full_check(wl, mode, cctas=4)
+
+
 def test_all_local_routing_sends_nothing():
     wl = Workload("all_local", W=4, L=2, topk=2, T=96, d_model=128, d_ff=256, tb_M=64, routing="balanced")
     inp = P.inputs_for(wl)

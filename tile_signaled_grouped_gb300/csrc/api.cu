@@ -53,7 +53,9 @@ int dims_from_cfg(const moe_cfg* c, Dims* d) {
   if (E > 1024 || c->topk < 1 || c->topk > std::min<long long>(E, 32)) return MOE_ERR_ARG;
   if (c->T < 1 || c->T > (1 << 20)) return MOE_ERR_ARG;
   if (c->d_model < 128 || c->d_model % 128 || c->d_ff < 128 || c->d_ff % 128) return MOE_ERR_ARG;
-  if (c->d_model > 16384 || c->d_ff > 65536) return MOE_ERR_UNSUPPORTED;  // a row fits one copy chunk
+  // A token row must fit one copy chunk (the combine copy moves whole rows through
+  // kChunkBytes shared-memory slots): d_model <= 10240.
+  if ((long long)c->d_model * 2 > kChunkBytes || c->d_ff > 65536) return MOE_ERR_UNSUPPORTED;
   if (c->tb_M != 64 && c->tb_M != 128 && c->tb_M != 256) return MOE_ERR_ARG;
   if (c->producer_pairs != 0 && c->producer_pairs != 1) return MOE_ERR_ARG;
   if (c->mgb < 1 || c->consumer_ctas < -1) return MOE_ERR_ARG;
