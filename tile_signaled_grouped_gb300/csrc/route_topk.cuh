@@ -87,6 +87,10 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
   static_assert(G == 1 || G == 32, "a thread or a whole warp per token");
   static_assert(PER <= 32, "candidates per lane");
   constexpr uint32_t kAll = 0xFFFFFFFFu;
+  // A warp's prescribed ids: lane j loads id j now, so that load overlaps the softmax
+  // instead of adding one memory round trip per round (k <= 32).
+  const int forced_mine =
+      (G > 1 && forced_row != nullptr && lig < k) ? __ldg(forced_row + lig) : -1;
   float mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < PER; ++i) mx = fmaxf(mx, vin[i]);
@@ -100,7 +104,7 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
 
   if (forced_row != nullptr) {
     for (int j = 0; j < k; ++j) {
-      const int e = __ldg(forced_row + j);
+      const int e = G > 1 ? __shfl_sync(kAll, forced_mine, j) : __ldg(forced_row + j);
       const bool in = e >= 0 && e < E;
       float ve = 0.f;
 #pragma unroll
