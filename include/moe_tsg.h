@@ -179,23 +179,29 @@ int moe_scale(moe_plan *plan, const float *topk_w, const void *const *recv, void
               moe_stream_t stream);
 
 /* Plan build that allocates nothing, for callers that cannot call cudaMalloc (for
- * example code running while a stream is captured into a CUDA graph, or a serving
- * loop that reserved all of its device memory up front). The pages have no
- * counterpart; it computes exactly what moe_plan_build computes (without the
- * layout gather), with the same kernels.
+ * example a serving loop that reserved all of its device memory up front, or a
+ * runtime whose device memory comes from an allocator it does not own). The pages
+ * have no counterpart. It runs moe_plan_build's plan kernels on the same routing
+ * and writes the same plan, but not the layout gather (X is not filled).
  *  topk_ids: [W][T][topk] int32 (input).
  *  plan_out: caller buffer of at least the plan_bytes of moe_workspace_size(),
- *            256-byte aligned; the plan arrays are written at the offsets
- *            moe_field() reports (MOE_PLAN_* fields). Bad routing ids set the
- *            MOE_PLAN_STATUS word inside plan_out, which this call never clears.
- * The kernels' internal scratch (token bitmaps, prefix counts, tile and segment
- * ordering) lives in a fixed 1 MiB array inside the library, which every GPU that
- * loads the library holds until the process exits; shapes whose scratch exceeds it
- * return MOE_ERR_UNSUPPORTED. No cudaMalloc, cudaFree or allocating library call
- * is made. The first call on each device looks up that array's device address
- * (cudaGetSymbolAddress, with the device current) and may load the library's
- * kernels: make it before any stream capture. Every call shares the one array, so
- * calls that overlap on the GPU (other streams, other threads) race; serialise them. */
+ *            256-byte aligned; the plan arrays are written where moe_plan_build
+ *            writes them in a plan workspace (moe_field() reports the public ones).
+ *            Bad routing ids set the MOE_PLAN_STATUS word inside plan_out, which
+ *            this call never clears. A plan handle created on plan_out
+ *            (moe_plan_create) can then run moe_expert_combine and moe_scale on it,
+ *            given rank workspaces whose X a moe_plan_build of the same routing
+ *            filled. The regions of the plan kernels' internal arrays (token
+ *            bitmaps, word prefixes, per-band and per-tile orderings, segment
+ *            indices) are left untouched in plan_out, as is the per-combine region.
+ * Those internal arrays live in a fixed 1 MiB array inside the library, which every
+ * GPU that loads the library holds until the process exits; shapes whose internal
+ * arrays exceed it return MOE_ERR_UNSUPPORTED. No cudaMalloc, cudaFree or
+ * allocating library call is made. The first call on each device looks up that
+ * array's device address (cudaGetSymbolAddress, with the device current) and may
+ * load the library's kernels: make it before any stream capture. Every call shares
+ * the one array, so calls that overlap on the GPU (other streams, other threads)
+ * race; serialise them. Host threads may make calls at the same time. */
 int moe_plan_build_noalloc(const moe_cfg *cfg, const int32_t *topk_ids, void *plan_out,
                            size_t plan_out_bytes, moe_stream_t stream);
 

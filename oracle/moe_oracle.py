@@ -66,8 +66,8 @@ import numpy as np
 
 __all__ = [
     "softmax", "silu", "round_bf16", "route", "gate_logits", "gate", "Plan", "build_plan",
-    "expert_ffn", "layout_rows", "rank_outputs", "buffer_row_outputs", "combine", "scale",
-    "forward", "padding_bound",
+    "expert_ffn", "expert_ffn_both", "layout_rows", "rank_outputs", "buffer_row_outputs",
+    "combine", "scale", "forward", "padding_bound",
 ]
 
 
@@ -373,6 +373,14 @@ def round_bf16(v) -> np.ndarray:
     return bits.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def _hidden(xrows, w_gate, w_up) -> np.ndarray:
+    """h = SiLU(W_gate x) * (W_up x) for each row x, float64, not rounded."""
+    x = np.asarray(xrows, dtype=np.float64)
+    g = x @ np.asarray(w_gate, dtype=np.float64).T
+    u = x @ np.asarray(w_up, dtype=np.float64).T
+    return silu(g) * u
+
+
 def expert_ffn(xrows, w_gate, w_up, w_down, round_hidden: bool = True) -> np.ndarray:
     """y = W_down h, h = SiLU(W_gate x) * (W_up x), for each row x.
 
@@ -380,13 +388,19 @@ def expert_ffn(xrows, w_gate, w_up, w_down, round_hidden: bool = True) -> np.nda
     float64 throughout; h is rounded to bf16 before the second GEMM (reading R11)
     unless round_hidden is False.
     """
-    x = np.asarray(xrows, dtype=np.float64)
-    g = x @ np.asarray(w_gate, dtype=np.float64).T
-    u = x @ np.asarray(w_up, dtype=np.float64).T
-    a = silu(g) * u
+    a = _hidden(xrows, w_gate, w_up)
     if round_hidden:
         a = round_bf16(a)
     return a @ np.asarray(w_down, dtype=np.float64).T
+
+
+def expert_ffn_both(xrows, w_gate, w_up, w_down):
+    """(expert_ffn with h rounded to bf16, expert_ffn with h unrounded) of the same
+    rows, computing h once: the half-precision reading R11 and the plain
+    float64 FFN side by side."""
+    a = _hidden(xrows, w_gate, w_up)
+    wd = np.asarray(w_down, dtype=np.float64).T
+    return round_bf16(a) @ wd, a @ wd
 
 
 def layout_rows(plan: Plan, x, o: int) -> np.ndarray:

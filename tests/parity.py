@@ -1,15 +1,40 @@
 """Helpers shared by the GPU parity tests: run the CUDA path, build the oracle's
 view of the same inputs, and compare element by element.
 
-Tolerance for floating-point results, against the float64 oracle: relative L2
-error <= 5e-3 and, per element, |got - want| <= max(2e-2, ulp_bf16(want)).
-The results are bf16 tensors. Where |want| >= 4 the spacing of bf16 values
-(one ulp) is >= 0.03125, so even the correctly rounded value can sit more than
-2e-2 away, and the path's two bf16 roundings (hidden activation, then output)
-can land one ulp away; there the bound is that one ulp. Below |want| = 2.56 the
-bound is the plain 2e-2.
+Tolerance for floating-point results, derived from the stated one (max-abs 2e-2
+and relative L2 5e-3 against the oracle) plus the rounding of the output:
+
+  * The path's results are bf16. Whatever fp32 value v the kernel accumulated,
+    the stored element is v rounded to the nearest bf16 value, which moves it by
+    at most half a bf16 spacing at |v|: ulp_bf16(|v|) / 2, where ulp_bf16(a) =
+    2^(floor(log2 a) - 7) (8 significant bits).
+  * A v within the stated 2e-2 of the oracle's value `want` has |v| <= |want| +
+    2e-2, so the stored element lies within
+
+        bound(want) = 2e-2 + ulp_bf16(|want| + 2e-2) / 2
+
+    of it. For |want| < 2 that is at most 0.0239, below 4 at most 0.0278, below 8
+    at most 0.0356, below 16 at most 0.0513.
+  * The stated max-abs 2e-2 alone is met wherever |want| < 4 on these workloads
+    (every A100-like and Qwen3-like element). It is not met by a bf16 output near
+    |want| = 8: the spacing of bf16 values there is 0.0625, so even a correctly
+    rounded result can sit 0.031 away. DeepSeek-V3-like (worst 0.034 at |y| =
+    8.15) and stress_skew (0.039 at |y| = 8.7) have such elements.
+
+Every comparison also checks relative L2 <= 5e-3 over the whole tensor. The
+oracle here rounds the hidden activation h to bf16 before the second GEMM
+(reading R11); beside it, the outputs are compared with the oracle that keeps h
+unrounded (the plain float64 FFN) at relative L2 <= 5e-3, and the assertion
+reports that comparison's max-abs.
+
+Canaries: every receive and output buffer sits between guard rows, and the rank
+workspaces start filled with a sentinel byte; after a run, the guards, the
+receive rows past the planned ones and the workspace rows past each owner's
+layout must still hold it (nothing is written outside the planned ranges).
 """
 from __future__ import annotations
+
+import dataclasses
 
 import numpy as np
 import torch
@@ -21,12 +46,24 @@ from tile_signaled_grouped_gb300.workloads import make_inputs
 
 MAX_ABS = 2e-2
 REL_L2 = 5e-3
+SENTINEL = 0xA5  # canary byte (bf16 0xA5A5 = -2.87e-16, not a value the path writes)
+GUARD = 8        # canary rows before and after each receive and output buffer
 
 
 def bf16_ulp(x) -> np.ndarray:
     """Spacing of bf16 values at |x| (8 significant bits)."""
     ax = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
     return np.exp2(np.floor(np.log2(ax)) - 7)
+
+
+def element_bound(want) -> np.ndarray:
+    """The stated max-abs plus the output's rounding (see the module docstring)."""
+    return MAX_ABS + 0.5 * bf16_ulp(np.abs(np.asarray(want, dtype=np.float64)) + MAX_ABS)
+
+
+def _rel_l2(got, want) -> float:
+    den = float(np.linalg.norm(want))
+    return float(np.linalg.norm(got - want)) / den if den > 0 else float(np.linalg.norm(got))
 
 
 def assert_close(got, want, what=""):
@@ -36,13 +73,23 @@ def assert_close(got, want, what=""):
     if got.size == 0:
         return
     err = np.abs(got - want)
-    bound = np.maximum(MAX_ABS, bf16_ulp(want))
+    bound = element_bound(want)
     worst = int(np.argmax(err / bound))
-    den = float(np.linalg.norm(want))
-    rel = float(np.linalg.norm(got - want)) / den if den > 0 else float(np.linalg.norm(got))
+    rel = _rel_l2(got, want)
     assert err.flat[worst] <= bound.flat[worst] and rel <= REL_L2, (
         f"{what}: max-abs {err.max():.3e}, worst {err.flat[worst]:.3e} at |want| "
         f"{abs(want.flat[worst]):.3f} (bound {bound.flat[worst]:.3e}), rel-L2 {rel:.3e}")
+
+
+def assert_close_unrounded(got, want_u, what=""):
+    """Against the oracle with h unrounded: relative L2 only, max-abs reported."""
+    got = np.asarray(got, dtype=np.float64)
+    want_u = np.asarray(want_u, dtype=np.float64)
+    if got.size == 0:
+        return
+    rel = _rel_l2(got, want_u)
+    assert rel <= REL_L2, (f"{what} vs the unrounded-h oracle: rel-L2 {rel:.3e}, "
+                           f"max-abs {np.abs(got - want_u).max():.3e}")
 
 
 def f64(t: torch.Tensor) -> np.ndarray:
@@ -50,13 +97,17 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().double().cpu().numpy()
 
 
-def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0, pairs=0):
+def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0, pairs=0, canaries=True):
     """The whole path through the C ABI. mode: 'overlap' (two streams), 'serial', or
     'fused' (the copy inside the pair producer); pairs: 1 runs the CTA-pair producer
-    (0, the default here, keeps the one-CTA producer under test)."""
+    (0, the default here, keeps the one-CTA producer under test). With canaries the
+    receive and output buffers get guard rows and the rank workspaces start filled
+    with the sentinel byte (check_canaries tests them after the run)."""
     cc = {"overlap": consumer_ctas, "serial": 0, "fused": -1}[mode]
     layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb,
                           cc, timeout_ns, 1 if mode == "fused" else pairs)
+    if canaries:
+        install_canaries(layer)
     sp = torch.cuda.Stream()
     sc = torch.cuda.Stream(priority=-1)
     torch.cuda.synchronize()
@@ -66,10 +117,54 @@ def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0, pairs=0):
     return layer
 
 
-def oracle_plan(wl, inp):
-    forced = None if inp.forced_ids is None else inp.forced_ids.cpu().numpy()
-    ids, w = O.route(inp.logits.cpu().numpy(), wl.topk, forced)
-    return ids, w, O.build_plan(ids, wl.W, wl.L, wl.tb_M, wl.mgb)
+def _guarded(rows, D, dev):
+    buf = torch.full((GUARD + rows + GUARD, D), 0, dtype=torch.bfloat16, device=dev)
+    buf.view(torch.uint8).fill_(SENTINEL)
+    return buf, buf[GUARD:GUARD + rows]
+
+
+def install_canaries(layer):
+    """Receive and output buffers between guard rows; rank workspaces all sentinel."""
+    layer._canary = {"recv": [], "out": []}
+    for s in range(layer.W):
+        buf, inner = _guarded(layer.recv[s].shape[0], layer.D, layer.device)
+        layer._canary["recv"].append(buf)
+        layer.recv[s] = inner
+        buf, inner = _guarded(layer.T, layer.D, layer.device)
+        layer._canary["out"].append(buf)
+        layer.out[s] = inner
+        layer._rank_raw[s].fill_(SENTINEL)
+
+
+def _untouched(t) -> bool:
+    return bool((t.contiguous().view(torch.uint8) == SENTINEL).all().item())
+
+
+def check_canaries(layer, wl, plan):
+    """Nothing outside the planned ranges was written: the guard rows of every receive
+    and output buffer, the receive rows past each rank's planned ones, and the rows of
+    each rank workspace past its layout (X past the 128-row boundary the gather
+    rounds to, h and Y past the layout's rows) still hold the sentinel."""
+    cv = getattr(layer, "_canary", None)
+    assert cv is not None, "run without canaries"
+    for s in range(wl.W):
+        buf = cv["recv"][s]
+        n = int(plan.recv_rows[s])
+        assert _untouched(buf[:GUARD]), f"guard rows before the receive buffer of rank {s}"
+        assert _untouched(buf[GUARD + n:]), f"receive buffer of rank {s} past row {n}"
+        buf = cv["out"][s]
+        assert _untouched(buf[:GUARD]) and _untouched(buf[GUARD + wl.T:]), f"output guards {s}"
+        rows = int(plan.rank_rows[s])
+        x_end = -(-rows // 128) * 128
+        X = layer.rank_field(capi.MOE_RANK_X, s)
+        H = layer.rank_field(capi.MOE_RANK_H, s)
+        Y = layer.rank_field(capi.MOE_RANK_Y, s)
+        assert _untouched(X[x_end:]), f"X rows of rank {s} past {x_end}"
+        assert _untouched(H[rows:]), f"h rows of rank {s} past {rows}"
+        assert _untouched(Y[rows:]), f"Y rows of rank {s} past {rows}"
+        raw, ws = layer._rank_raw[s], layer.rank_ws[s]
+        lo = ws.data_ptr() - raw.data_ptr()
+        assert _untouched(raw[:lo]) and _untouched(raw[lo + ws.numel():]), f"workspace {s}"
 
 
 def check_plan(layer, wl, plan, ids, w, w_rtol=2e-6):
@@ -171,17 +266,94 @@ def check_pairs(layer, wl, plan):
             assert bool(info >> 16) == above, "pair record: partner side"
 
 
-def check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=None, rng=None):
-    """X bit-exact; Y of valid rows within tolerance and exactly 0 on padding rows;
-    receive buffers an exact copy of Y rows; outputs within tolerance.
-    sample: None for every row/token, else the number sampled per rank."""
-    W, T, D = wl.W, wl.T, wl.d_model
-    rng = rng or np.random.default_rng(0)
-    wg = [_LazyExperts(t) for t in inp.w_gate]
-    wu = [_LazyExperts(t) for t in inp.w_up]
-    wd = [_LazyExperts(t) for t in inp.w_down]
+class RowStore:
+    """One owner's expert-output buffer [rows, D], held only at the rows that carry a
+    token (every other row of the layout is a zero row). Indexable like the full
+    array by a row or a slice of rows, which is all the oracle's combine and scale do."""
+
+    def __init__(self, nrows, rows, vals):
+        self.shape = (int(nrows), vals.shape[1])
+        self.rows = np.asarray(rows, dtype=np.int64)
+        self.vals = vals
+        self.pos = np.full(int(nrows), -1, dtype=np.int64)
+        self.pos[self.rows] = np.arange(len(self.rows))
+
+    def __getitem__(self, i):
+        if isinstance(i, slice):
+            p = self.pos[i]
+            out = np.zeros((len(p), self.shape[1]), dtype=np.float64)
+            m = p >= 0
+            out[m] = self.vals[p[m]]
+            return out
+        p = self.pos[int(i)]
+        return self.vals[p] if p >= 0 else np.zeros(self.shape[1], dtype=np.float64)
+
+
+@dataclasses.dataclass
+class OracleRun:
+    """The oracle's whole path on one workload's inputs: routing, plan, the expert
+    outputs of every token row of every owner (h rounded to bf16, and unrounded),
+    the receive buffers and the outputs of both."""
+    ids: np.ndarray
+    w: np.ndarray
+    plan: O.Plan
+    Y: list          # [W] RowStore, h rounded (reading R11)
+    Yu: list         # [W] RowStore, h unrounded
+    recv: list       # [W] [recv_rows, D]
+    out: list        # [W] [T, D]
+    out_u: list      # [W] [T, D] from Yu
+
+
+def oracle_run(wl, inp, routing=None) -> OracleRun:
+    """Every token row at every size: each expert's rows go through the oracle's FFN
+    in one call (weights copied to float64 one expert at a time). routing: (ids, w)
+    to use instead of the oracle's routing of the workload's gate logits."""
+    if routing is None:
+        ids, w, plan = oracle_plan(wl, inp)
+    else:
+        ids, w = routing
+        plan = O.build_plan(ids, wl.W, wl.L, wl.tb_M, wl.mgb)
     xs = [f64(t) for t in inp.x]
-    ycache = {}
+    T = wl.T
+    Y, Yu = [], []
+    for o in range(wl.W):
+        xsrc = plan.xsrc[o]
+        rows_all, vals, vals_u = [], [], []
+        for li in range(wl.L):
+            e = o * wl.L + li
+            lo = int(plan.expert_start[e])
+            hi = lo + int(plan.rows_alloc[e])
+            r = lo + np.nonzero(xsrc[lo:hi] >= 0)[0]
+            if not len(r):
+                continue
+            X = np.stack([xs[int(v) // T][int(v) % T] for v in xsrc[r]])
+            yr, yu = O.expert_ffn_both(X, f64(inp.w_gate[o][li]), f64(inp.w_up[o][li]),
+                                       f64(inp.w_down[o][li]))
+            rows_all.append(r)
+            vals.append(yr)
+            vals_u.append(yu)
+        D = wl.d_model
+        rows_all = np.concatenate(rows_all) if rows_all else np.zeros(0, dtype=np.int64)
+        cat = lambda v: np.concatenate(v) if v else np.zeros((0, D))
+        Y.append(RowStore(plan.rank_rows[o], rows_all, cat(vals)))
+        Yu.append(RowStore(plan.rank_rows[o], rows_all, cat(vals_u)))
+    recv = O.combine(plan, Y)
+    out = O.scale(plan, w, recv, Y)
+    out_u = O.scale(plan, w, O.combine(plan, Yu), Yu)
+    return OracleRun(ids, w, plan, Y, Yu, recv, out, out_u)
+
+
+def check_layout_and_outputs(layer, wl, inp, orc: OracleRun, canaries=True):
+    """Complete comparison of one run with the oracle, every row and every token:
+    X bit-exact (token rows copied, every other row zero); Y of every token row within
+    the tolerance and exactly 0 on every other row; every receive row a bit-exact copy
+    of its owner's Y row and within the tolerance of the oracle's combine; every
+    output token within the tolerance of the oracle, and of the unrounded-h oracle at
+    relative L2; the canaries intact (a fresh layer's first run only)."""
+    W, T, D = wl.W, wl.T, wl.d_model
+    plan = orc.plan
+    dev = layer.out[0].device
+    xall = torch.cat([t.view(T, D) for t in inp.x])  # [W*T, D]: row s*T+t
     for o in range(W):
         rows_n = int(plan.rank_rows[o])
         X = layer.rank_field(capi.MOE_RANK_X, o)[:rows_n]
@@ -189,75 +361,46 @@ def check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=None, rng=None
         xsrc = plan.xsrc[o]
         valid = np.nonzero(xsrc >= 0)[0]
         pad = np.nonzero(xsrc < 0)[0]
-        # X: copies of token rows, zero rows elsewhere (bit-exact)
-        if sample is None:
-            sel = valid
-        else:
-            sel = np.sort(rng.choice(valid, size=min(sample, len(valid)), replace=False))
-        Xs = X[torch.as_tensor(sel, device=X.device)].cpu() if len(sel) else None
-        for n, r in enumerate(sel):
-            s, t = divmod(int(xsrc[r]), T)
-            assert torch.equal(Xs[n], inp.x[s][t].cpu()), f"X row {r} of rank {o}"
+        assert np.array_equal(valid, orc.Y[o].rows), "oracle rows"
+        vt = torch.as_tensor(valid, device=dev)
+        if len(valid):
+            src = torch.as_tensor(xsrc[valid], device=dev)
+            assert torch.equal(X[vt], xall[src]), f"X token rows of rank {o}"
         if len(pad):
-            pt = torch.as_tensor(pad, device=X.device)
+            pt = torch.as_tensor(pad, device=dev)
             assert not X[pt].any().item(), f"padding rows of X, rank {o}"
             assert not Y[pt].any().item(), f"padding rows of Y must be exactly 0, rank {o}"
-        if len(sel):
-            want = O.buffer_row_outputs(plan, xs, wg, wu, wd, o, sel)
-            got = f64(Y[torch.as_tensor(sel, device=Y.device)])
-            assert_close(got, want, f"Y rank {o}")
-            for r, y in zip(sel.tolist(), want):
-                ycache[(o, r)] = y
-    # Combine: receive rows are exact copies of the owner's Y rows.
+        if len(valid):
+            assert_close(f64(Y[vt]), orc.Y[o].vals, f"Y rank {o}")
+    # Combine: receive rows are bit-exact copies of the owner's Y rows, gathered per
+    # (owner, destination) group, and match the oracle's receive buffers.
     for o in range(W):
         Y = layer.rank_field(capi.MOE_RANK_Y, o)
+        src_rows = {s_: [] for s_ in range(W)}
+        dst_rows = {s_: [] for s_ in range(W)}
         for b in range(len(plan.band_expert[o])):
             dst = int(plan.band_dst[o][b])
             if dst == o:
                 continue
             v, r0 = int(plan.band_valid[o][b]), int(plan.band_dst_row[o][b])
-            assert torch.equal(layer.recv[dst][r0:r0 + v], Y[b * wl.tb_M:b * wl.tb_M + v]), \
-                f"combine copy of band {b} of rank {o}"
-    # Scale: per token sum over its k experts, evaluated expert by expert.
-    picks = {}
+            src_rows[dst].append(np.arange(b * wl.tb_M, b * wl.tb_M + v))
+            dst_rows[dst].append(np.arange(r0, r0 + v))
+        for dst in range(W):
+            if not src_rows[dst]:
+                continue
+            a = torch.as_tensor(np.concatenate(dst_rows[dst]), device=dev)
+            b_ = torch.as_tensor(np.concatenate(src_rows[dst]), device=dev)
+            assert torch.equal(layer.recv[dst][a], Y[b_]), f"combine copy {o} -> {dst}"
     for s_ in range(W):
-        toks = np.arange(T) if sample is None else np.sort(
-            rng.choice(T, size=min(sample, T), replace=False))
-        picks[s_] = toks
-    need = {}
-    for s_, toks in picks.items():
-        for t in toks.tolist():
-            for j in range(wl.topk):
-                need.setdefault(int(ids[s_, t, j]), []).append((s_, t, j))
-    yv = {}
-    for e in sorted(need):
-        o, li = divmod(e, wl.L)
-        rows = np.stack([xs[s_][t] for s_, t, _ in need[e]])
-        ys = O.expert_ffn(rows, wg[o][li], wu[o][li], wd[o][li])
-        for key, y in zip(need[e], ys):
-            yv[key] = y
-    for s_, toks in picks.items():
-        got = f64(layer.out[s_][torch.as_tensor(toks, device=layer.out[s_].device)])
-        want = np.zeros_like(got)
-        for n, t in enumerate(toks.tolist()):
-            for j in range(wl.topk):
-                want[n] += w[s_, t, j] * yv[(s_, t, j)]
-        assert_close(got, want, f"out rank {s_}")
-
-
-class _LazyExperts:
-    """Per-expert float64 copies of one rank's weight tensor, made on first use."""
-
-    def __init__(self, t: torch.Tensor):
-        self.t = t
-        self.cache = {}
-
-    def __getitem__(self, li):
-        if li not in self.cache:
-            if len(self.cache) > 2:
-                self.cache.clear()
-            self.cache[li] = f64(self.t[li])
-        return self.cache[li]
+        n = int(plan.recv_rows[s_])
+        assert_close(f64(layer.recv[s_][:n]), orc.recv[s_], f"receive buffer of rank {s_}")
+    # Scale: every token of every rank.
+    for s_ in range(W):
+        got = f64(layer.out[s_])
+        assert_close(got, orc.out[s_], f"out rank {s_}")
+        assert_close_unrounded(got, orc.out_u[s_], f"out rank {s_}")
+    if canaries and getattr(layer, "_canary", None) is not None:
+        check_canaries(layer, wl, plan)
 
 
 def inputs_for(wl):

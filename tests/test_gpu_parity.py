@@ -1,12 +1,13 @@
 """Parity of the CUDA path against the CPU oracle, through the C ABI.
 
 Plan arrays (layout, schedule, combine plan, segments, scale map) and the
-layout gather and combine copies are compared bit-exactly; FFN rows and the
-final outputs within max-abs 2e-2 and relative L2 5e-3 of the float64 oracle.
+layout gather and combine copies are compared bit-exactly; every FFN row and
+every output token within the tolerance of tests/parity.py (the stated max-abs
+2e-2 plus the bf16 rounding of the output, relative L2 5e-3). The workload
+shapes at full size are in test_gpu_full_size.py.
 """
 import dataclasses
 
-import numpy as np
 import pytest
 import torch
 
@@ -21,10 +22,10 @@ def _full_check(wl, mode="overlap", cctas=8):
     inp = P.inputs_for(wl)
     layer = P.run_gpu(wl, inp, mode=mode, consumer_ctas=cctas)
     assert layer.status() == (0, 0)
-    ids, w, plan = P.oracle_plan(wl, inp)
-    P.check_plan(layer, wl, plan, ids, w)
-    P.check_order(layer, wl, plan)
-    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w)
+    orc = P.oracle_run(wl, inp)
+    P.check_plan(layer, wl, orc.plan, orc.ids, orc.w)
+    P.check_order(layer, wl, orc.plan)
+    P.check_layout_and_outputs(layer, wl, inp, orc)
     layer.close()
 
 
@@ -70,30 +71,13 @@ def test_all_local_routing_sends_nothing():
     inp.forced_ids = torch.stack([ids, ids + 1], dim=-1).cuda()
     layer = P.run_gpu(wl, inp)
     assert layer.status() == (0, 0)
-    ids_o, w, plan = P.oracle_plan(wl, inp)
-    assert plan.recv_rows.sum() == 0
-    P.check_plan(layer, wl, plan, ids_o, w)
-    P.check_layout_and_outputs(layer, wl, inp, plan, ids_o, w)
+    orc = P.oracle_run(wl, inp)
+    assert orc.plan.recv_rows.sum() == 0
+    P.check_plan(layer, wl, orc.plan, orc.ids, orc.w)
+    P.check_layout_and_outputs(layer, wl, inp, orc)
 
 
 FULL = ["a100_like", "qwen3_235b_like", "deepseek_v3_like", "stress_skew"]
-
-
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
-    """The workload shapes at full size with the one-CTA producer and the consumer
-    kernel overlapped on two streams: every plan array bit-exact, sampled rows and
-    tokens against the oracle, all copies exact. (The schedule the bench times, the
-    fused pair producer, is covered in test_gpu_pairs.py.)"""
-    wl = get_workload(name)
-    inp = P.inputs_for(wl)
-    layer = P.run_gpu(wl, inp, mode="overlap", consumer_ctas=16)
-    assert layer.status() == (0, 0)
-    ids, w, plan = P.oracle_plan(wl, inp)
-    P.check_plan(layer, wl, plan, ids, w)
-    P.check_order(layer, wl, plan)
-    P.check_layout_and_outputs(layer, wl, inp, plan, ids, w, sample=12,
-                               rng=np.random.default_rng(1))
 
 
 def test_repeat_runs_are_identical():
@@ -212,7 +196,7 @@ def test_layout_changes_between_builds(mode):
                       producer=sp, consumer=sc)
         torch.cuda.synchronize()
         assert layer.status() == (0, 0)
-        ids, wt, plan = P.oracle_plan(base, inp)
-        P.check_plan(layer, base, plan, ids, wt)
-        P.check_layout_and_outputs(layer, base, inp, plan, ids, wt)
+        orc = P.oracle_run(base, inp)
+        P.check_plan(layer, base, orc.plan, orc.ids, orc.w)
+        P.check_layout_and_outputs(layer, base, inp, orc)
     layer.close()

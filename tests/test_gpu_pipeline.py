@@ -119,9 +119,9 @@ def test_tuned_schedule_keeps_results_exact():
     torch.cuda.synchronize()
     assert layer.status() == (0, 0)
     wl_t = dataclasses.replace(wl, mgb=mgb)
-    ids, w, plan = P.oracle_plan(wl_t, inp)
-    P.check_plan(layer, wl_t, plan, ids, w)
-    P.check_layout_and_outputs(layer, wl_t, inp, plan, ids, w)
+    orc = P.oracle_run(wl_t, inp)
+    P.check_plan(layer, wl_t, orc.plan, orc.ids, orc.w)
+    P.check_layout_and_outputs(layer, wl_t, inp, orc)
     with pytest.raises(capi.MoeError, match="ARG"):
         layer.set_schedule(-3, 1)
     with pytest.raises(capi.MoeError, match="ARG"):

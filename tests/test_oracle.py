@@ -167,6 +167,24 @@ def test_ffn_rounds_the_hidden_activation():
     np.testing.assert_allclose(O.expert_ffn(x, one, one, one, round_hidden=False), [[h]], rtol=1e-15)
 
 
+def test_ffn_both_roundings_from_one_hidden_activation():
+    """expert_ffn_both gives the two readings of the hidden activation: the hand value
+    above (h = 3.5232 rounds to 3.515625) and the unrounded h, and on random rectangular
+    operands the same rows as expert_ffn with and without the rounding."""
+    x, one = np.array([[2.0]]), np.array([[1.0]])
+    r, u = O.expert_ffn_both(x, one, one, 2 * one)
+    assert r[0, 0] == 7.03125
+    np.testing.assert_allclose(u, [[8.0 / (1.0 + np.exp(-2.0))]], rtol=1e-15)
+    rng = np.random.default_rng(4)
+    xr = rng.standard_normal((5, 3))
+    wg, wu, wd = (rng.standard_normal(s) for s in ((4, 3), (4, 3), (3, 4)))
+    r, u = O.expert_ffn_both(xr, wg, wu, wd)
+    np.testing.assert_allclose(r, O.expert_ffn(xr, wg, wu, wd), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(u, O.expert_ffn(xr, wg, wu, wd, round_hidden=False), rtol=0,
+                               atol=1e-13)
+    assert np.abs(r - u).max() > 0  # the rounding is applied to one of them only
+
+
 # ---------------------------------------------------------------- layout / schedule / plan
 
 def test_worked_example_figure2():

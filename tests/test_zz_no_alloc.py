@@ -1,12 +1,15 @@
 """moe_plan_build_noalloc: the plan build for callers that cannot allocate device
-memory (code running under CUDA-graph capture, or serving loops that reserved all
-of their memory up front). It must produce exactly the plan that moe_plan_build
-produces for the same routing, call after call, although its internal scratch is
-a fixed array inside the library that every call reuses.
+memory (a serving loop that reserved all of its memory up front, or a runtime
+whose device memory comes from an allocator it does not own). It must produce
+exactly the plan that moe_plan_build produces for the same routing, call after
+call, although its internal scratch is a fixed array inside the library that
+every call reuses; and that plan must drive moe_expert_combine and moe_scale.
 
 Kept in a file of its own that pytest collects last."""
 import pytest
 import torch
+
+from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
@@ -86,6 +89,64 @@ def _compare_prefixes(ref, out, wl):
     for f, n in [("MOE_PLAN_TILE_ROW", tot[0]), ("MOE_PLAN_TILE_EXPERT", tot[0]),
                  ("MOE_PLAN_SEG_ORDER", tot[1]), ("MOE_PLAN_PAIR", 4 * tot[5])]:
         assert torch.equal(view(f)[:n], ref.field(capi.ENUMS[f])[:n]), f
+
+
+def _plan_buffer(layer):
+    """A plan workspace holding garbage except a clear status word (an output of the call)."""
+    buf = torch.full((layer.plan_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+    off, cnt = capi.moe_field(layer.cfg, capi.MOE_PLAN_STATUS)
+    buf[off:off + 4 * cnt] = 0
+    return buf
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_235b_like"])
+def test_noalloc_plan_drives_the_combine_on_two_calls_in_a_row(name):
+    """A plan workspace filled only by moe_plan_build_noalloc runs moe_expert_combine and
+    moe_scale (on rank workspaces whose X a moe_plan_build of the same routing filled):
+    the receive buffers and outputs equal the regular path's bit for bit and the
+    oracle's within the parity tolerance, for two different routings in a row into the
+    same buffer. The second call allocates no device memory."""
+    plan2 = handle = None
+    for call, seed in enumerate([0, 7]):
+        wl = get_workload(name, seed=seed)
+        inp = P.inputs_for(wl)
+        torch.cuda.synchronize()
+        ref = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb)
+        sp, sc = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+        ref.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                    producer=sp, consumer=sc)
+        torch.cuda.synchronize()
+        assert ref.status() == (0, 0)
+        if plan2 is None:
+            plan2 = _plan_buffer(ref)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        capi.moe_plan_build_noalloc(ref.cfg, ref.ids.data_ptr(), plan2.data_ptr(), ref.plan_bytes,
+                                    sp.cuda_stream)
+        torch.cuda.synchronize()
+        if call > 0:
+            assert torch.cuda.mem_get_info()[0] == free0, "the call allocated device memory"
+        handle = capi.moe_plan_create(ref.cfg, plan2.data_ptr(), ref.plan_bytes,
+                                      [t.data_ptr() for t in ref.rank_ws], ref.rank_bytes)
+        recv2 = [torch.full_like(r, 7.0) for r in ref.recv]
+        out2 = [torch.full_like(o, 7.0) for o in ref.out]
+        capi.moe_expert_combine(handle, [t.data_ptr() for t in inp.w_gate],
+                                [t.data_ptr() for t in inp.w_up],
+                                [t.data_ptr() for t in inp.w_down],
+                                [t.data_ptr() for t in recv2], sp.cuda_stream, sc.cuda_stream)
+        capi.moe_scale(handle, ref.w.data_ptr(), [t.data_ptr() for t in recv2],
+                       [t.data_ptr() for t in out2], sp.cuda_stream)
+        assert capi.moe_status(handle, sp.cuda_stream) == (0, 0)
+        torch.cuda.synchronize()
+        capi.moe_plan_destroy(handle)
+        rr = ref.field(capi.MOE_PLAN_RECV_ROWS).tolist()
+        for s_ in range(wl.W):
+            assert torch.equal(recv2[s_][:rr[s_]], ref.recv[s_][:rr[s_]]), f"call {call} recv {s_}"
+            assert torch.equal(out2[s_], ref.out[s_]), f"call {call} out {s_}"
+        orc = P.oracle_run(wl, inp)
+        for s_ in range(wl.W):
+            P.assert_close(P.f64(out2[s_]), orc.out[s_], f"call {call} out rank {s_}")
+        ref.close()
 
 
 def test_noalloc_rejects_what_it_cannot_hold():

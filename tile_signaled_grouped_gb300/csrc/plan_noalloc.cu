@@ -1,14 +1,16 @@
 // Plan build for callers that cannot allocate device memory.
 //
-// Some callers may not call cudaMalloc: code that runs while a stream is being
-// captured into a CUDA graph (allocation is not permitted during capture), or a
-// serving loop that reserved all of its device memory up front and forbids
-// allocation afterwards. moe_plan_build needs a caller-provided workspace that
-// holds both the plan and the plan kernels' internal scratch (token bitmaps,
-// popcount prefixes, tile and segment ordering, consumer records). This variant
-// runs the same plan kernels, but keeps that internal scratch in a file-scope
-// device array of fixed size; the caller passes only the routing ids (input)
-// and a buffer for the plan arrays (output).
+// Some callers may not call cudaMalloc: a serving loop that reserved all of its
+// device memory up front and forbids allocation afterwards, or a runtime whose
+// allocator belongs to someone else (an inference server handing out fixed
+// arenas). moe_plan_build needs a caller-provided workspace that holds both the
+// plan and the plan kernels' internal scratch (token bitmaps, popcount prefixes,
+// tile ordering, segment indices). This variant runs the same plan kernels, but
+// keeps that internal scratch in a file-scope device array of fixed size; the
+// caller passes only the routing ids (input) and a buffer for the plan arrays
+// (output), and every array that moe_expert_combine and moe_scale read lands in
+// that buffer.
+#include <atomic>
 #include <cstring>
 
 #include "moe_common.cuh"
@@ -23,18 +25,21 @@ namespace {
 constexpr size_t kScratchBytes = 1u << 20;
 static __device__ __align__(256) uint8_t g_plan_scratch[kScratchBytes];
 
-// Plan-workspace arrays that the plan kernels use internally. They live in the
-// static scratch; every other array is written to the caller's output buffer at
-// the offset moe_field() reports.
-constexpr int kInternal[] = {PA_BITMAP,   PA_WPRE,       PA_NB,         PA_RANK_NB,
-                             PA_BAND_TILE, PA_SEG_GIDX,  PA_GROUP_NSEG, PA_RANK_TILES,
-                             PA_UNIT_BEGIN, PA_SEG_REC,  PA_GROUP_NCHUNK};
+// Plan-workspace arrays that only the plan kernels themselves read. They live in
+// the static scratch; every other array (among them everything the producer, the
+// consumer and the scale read: tile list, scheduling units, CTA pairs, segment
+// records, chunk counts per group, scale map) is written to the caller's output
+// buffer at its moe_plan_build offset.
+constexpr int kInternal[] = {PA_BITMAP,    PA_WPRE,     PA_NB,         PA_RANK_NB,
+                             PA_BAND_TILE, PA_SEG_GIDX, PA_GROUP_NSEG, PA_RANK_TILES};
 
 constexpr int kMaxDevices = 64;
 // Device address of g_plan_scratch per device ordinal, looked up by the first
 // call made with that device current. In host code the array's name is only a
-// host-side stand-in, so kernels must receive this address instead.
-void* g_scratch_addr[kMaxDevices] = {};
+// host-side stand-in, so kernels must receive this address instead. Atomic, so
+// host threads that make their first calls at the same time do not race on it
+// (each stores the same address).
+std::atomic<void*> g_scratch_addr[kMaxDevices] = {};
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -62,13 +67,13 @@ extern "C" int moe_plan_build_noalloc(const moe_cfg* cfg, const int32_t* topk_id
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || p == nullptr)
+  void* addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (addr == nullptr) {
+    if (cudaGetSymbolAddress(&addr, g_plan_scratch) != cudaSuccess || addr == nullptr)
       return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(addr, std::memory_order_release);
   }
-  uint8_t* scratch = static_cast<uint8_t*>(g_scratch_addr[dev]);
+  uint8_t* scratch = static_cast<uint8_t*>(addr);
   uint8_t* out = static_cast<uint8_t*>(plan_out);
 
   DevPlan dp;
@@ -79,6 +84,10 @@ extern "C" int moe_plan_build_noalloc(const moe_cfg* cfg, const int32_t* topk_id
   dp.timeout_ns = cfg->timeout_ns > 0 ? cfg->timeout_ns : 2000000000LL;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // A launch error is read back with cudaGetLastError after the launches; take any
+  // error left pending by earlier, unrelated calls first, so it is not reported as
+  // this call's.
+  (void)cudaGetLastError();
   // The scratch keeps the previous call's contents: the token bitmaps must start at
   // zero (every other internal array is fully rewritten by the plan kernels).
   if (cudaMemsetAsync(dp.a[PA_BITMAP], 0, cnt[PA_BITMAP] * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
