@@ -167,6 +167,12 @@ def check_canaries(layer, wl, plan):
         assert _untouched(raw[:lo]) and _untouched(raw[lo + ws.numel():]), f"workspace {s}"
 
 
+def oracle_plan(wl, inp):
+    forced = None if inp.forced_ids is None else inp.forced_ids.cpu().numpy()
+    ids, w = O.route(inp.logits.cpu().numpy(), wl.topk, forced)
+    return ids, w, O.build_plan(ids, wl.W, wl.L, wl.tb_M, wl.mgb)
+
+
 def check_plan(layer, wl, plan, ids, w, w_rtol=2e-6):
     """Every plan array bit-exact against the oracle; the gate weights within w_rtol."""
     W, L, E = wl.W, wl.L, wl.E
