@@ -176,7 +176,8 @@ def gpu_arm(args, rank, world, local_rank):
     # expert FFN. Every step still runs the whole path on its own batch.
     n_fly = max(1, args.batches_in_flight)
     layers = [ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas,
-                            producer_pairs=args.producer_pairs) for _ in range(n_fly)]
+                            producer_pairs=args.producer_pairs, scale_mode=args.scale)
+              for _ in range(n_fly)]
     layer = layers[0]
     sps = [torch.cuda.Stream() for _ in range(n_fly)]
     scs = [torch.cuda.Stream(priority=-1) for _ in range(n_fly)]
@@ -206,10 +207,11 @@ def gpu_arm(args, rank, world, local_rank):
     flops_valid = 6.0 * valid_rows * D * F
 
     # ---- timed region: K steps, inputs resident in HBM ------------------------------
-    # The library records CUDA events around each of its kernels on the kernel's own
-    # stream (no host synchronisation inside the region); their means give the
-    # producer's launch time for the roofline.
-    layer.set_timing(True)
+    # The library keeps device-clock records of each combine (timing mode 2: no CUDA
+    # event enters the streams, so kernels overlap exactly as untimed): the producer's
+    # execution span for the roofline, the overlapped scale's span, and when each
+    # combine copy chunk landed.
+    layer.set_timing(2)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
@@ -235,6 +237,7 @@ def gpu_arm(args, rank, world, local_rank):
             torch.distributed.barrier()
         wall = time.perf_counter() - t_wall
     kernel_ms = layer.timings()
+    landed, tail_us, copy_bytes = layer.combine_overlap()
     layer.set_timing(False)
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, device="cuda")
     for lay in layers:
@@ -259,7 +262,7 @@ def gpu_arm(args, rank, world, local_rank):
     # The producer's execution span on the device clock (first CTA start to last CTA
     # end): with batches in flight, the event pair around a launch also counts the time
     # the kernel waits for the previous batch's producer to leave the SMs.
-    prod_avg = kernel_ms[6] if kernel_ms[6] > 0 else kernel_ms[2]
+    prod_avg = kernel_ms[6]
     achieved = flops_exec / (prod_avg * 1e-3) / 1e12
     # Consecutive producer spans overlap a little (the next batch's producer starts as
     # the previous one drains), so the span rate is beside the rate per step: the
@@ -291,6 +294,8 @@ def gpu_arm(args, rank, world, local_rank):
                                 else "overlapped (consumer kernel on its own SMs)"),
                    "producer": "CTA pairs (cta_group::2, M=256)" if args.producer_pairs
                    else "one CTA per tile (M=128)",
+                   "scale": ("overlapped with the producer (moe_scale_gated)"
+                             if args.scale == "gated" else "after the combine (moe_scale)"),
                    "producer_ctas": launch[0], "consumer_ctas_launched": launch[1],
                    "num_sms": launch[2], "pair_clusters_resident": launch[3],
                    "parallelism": f"{W} logical EP ranks on 1 GPU; replicas x{world}",
@@ -304,9 +309,7 @@ def gpu_arm(args, rank, world, local_rank):
                                      "burst below 1 s, sustained above)"),
                      "flops_per_launch": flops_exec, "launch_ms": prod_avg,
                      "launch_ms_source": ("device-clock span of each producer launch (first CTA "
-                                          "start to last CTA end), mean over the timed region"
-                                          if kernel_ms[6] > 0 else
-                                          "CUDA events around each producer launch"),
+                                          "start to last CTA end), mean over the timed region"),
                      "per_step_tflops": per_step, "per_step_frac": per_step / peak,
                      "per_step_source": "executed FLOPs of one step / ms_per_step"},
         "e2e": e2e,
@@ -318,9 +321,14 @@ def gpu_arm(args, rank, world, local_rank):
                  "tflop_executed": flops_exec / 1e12, "tflop_valid": flops_valid / 1e12,
                  "recv_rows": recv_rows},
         "timed_wall_s": wall,
-        "kernel_ms_in_timed_region": dict(zip(
-            ["route", "plan", "producer", "consumer", "scale", "gather", "producer_span"],
-            kernel_ms)),
+        "device_clock_ms_in_timed_region": {
+            "producer_span": kernel_ms[6], "gated_scale_span": kernel_ms[7],
+            "gated_scale_before_producer_end": kernel_ms[8]},
+        # TileMoE notes 7.3: how much of the second all-to-all the FFN hides. Here: the
+        # share of the combine's bytes whose copies had landed when the producer
+        # finished its last output tile (last combine of the timed region).
+        "combine_overlap": {"landed_before_last_tile": landed, "last_copy_after_last_tile_us": tail_us,
+                            "copy_bytes": copy_bytes},
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
@@ -479,6 +487,40 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         sweep[str(cc)] = ev0.elapsed_time(ev1) / (iters * 4)
         lay.close()
         del lay
+    # Scale after the combine or overlapped with it (moe_scale_gated), with one batch at
+    # a time or two in flight: whole-step time of each.
+    scale_sweep = {}
+    for n_fly in (1, 2):
+        for mode in ("after", "gated"):
+            lays = [ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, args.consumer_ctas,
+                                  producer_pairs=args.producer_pairs, scale_mode=mode)
+                    for _ in range(n_fly)]
+            sps = [sp] + [torch.cuda.Stream() for _ in range(n_fly - 1)]
+            scs = [sc] + [torch.cuda.Stream(priority=-1) for _ in range(n_fly - 1)]
+
+            def run(i):
+                lays[i % n_fly].forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits,
+                                        inp.forced_ids, producer=sps[i % n_fly],
+                                        consumer=scs[i % n_fly])
+
+            for i in range(3 * n_fly):
+                run(i)
+            torch.cuda.synchronize()
+            ev0.record(sp)
+            for s_ in sps[1:]:
+                s_.wait_event(ev0)
+            for i in range(iters * 4):
+                run(i)
+            for s_ in sps[1:]:
+                sp.wait_stream(s_)
+            ev1.record(sp)
+            torch.cuda.synchronize()
+            for lay in lays:
+                if lay.status() != (0, 0):
+                    raise RuntimeError(f"device status {lay.status()} in the scale sweep")
+                lay.close()
+            scale_sweep[f"{mode}_x{n_fly}"] = ev0.elapsed_time(ev1) / (iters * 4)
+            del lays
     # The same step captured once into a CUDA graph and replayed (one host launch per step).
     layer.set_timing(False)
     graph = layer.capture(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
@@ -510,6 +552,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         "overlapped_ms": over,
         "serial_ms": ser,
         "step_ms_by_consumer_ctas": sweep,
+        "step_ms_by_scale_and_batches_in_flight": scale_sweep,
         "step_ms_graph_replay": graph_ms,
         "producer_alone_tflops": flops / (ser["producer"] * 1e-3) / 1e12,
         "producer_alone_frac_burst": flops / (ser["producer"] * 1e-3) / 1e12 / bf16,
@@ -525,7 +568,8 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
                              "(512 MB write) before the routing, the plan build (the gather "
                              "is its last kernel), the producer and the scale; the consumer "
                              "follows the producer on one stream with no flush between them"),
-        "scale_in_step_gbs": scale_bytes / (over["scale"] * 1e-3) / 1e9,
+        "scale_in_step_gbs": (scale_bytes / (over["scale"] * 1e-3) / 1e9
+                              if over["scale"] > 0 else None),  # no events around a gated scale
         "gather_in_step_gbs": gather_bytes / (over["gather"] * 1e-3) / 1e9,
         "gate": gate,
     }
@@ -655,6 +699,10 @@ def main():
     ap.add_argument("--batches-in-flight", type=int, default=2,
                     help="layer instances (own plan and workspaces) that take steps in turn, so "
                          "one batch's routing, plan and gather overlap the previous batch's FFN")
+    ap.add_argument("--scale", default="after", choices=["after", "gated"],
+                    help="after: moe_scale once the combine is done; gated: moe_scale_gated, "
+                         "launched behind the producer, waits on the device for each token's "
+                         "group signals and ready flags")
     ap.add_argument("--producer-pairs", type=int, default=1, choices=[0, 1],
                     help="1: the CTA-pair producer (clusters of two, tcgen05 cta_group::2)")
     ap.add_argument("--gate-only", action="store_true",

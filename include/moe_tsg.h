@@ -178,6 +178,35 @@ int moe_expert_combine(moe_plan *plan, const void *const *w_gate, const void *co
 int moe_scale(moe_plan *plan, const float *topk_w, const void *const *recv, void *const *out,
               moe_stream_t stream);
 
+/* Scale overlapped with the combine (TileMoE notes section 2.2 step 5; the Perseus
+ * summary, section 4.1, Algorithm 1: the receiver acts on the one signal of each
+ * (sender, destination) group). Same arguments and the same results, bit for bit,
+ * as moe_scale, for the routing of the last moe_expert_combine. Enqueue it on that
+ * call's producer stream right after it: the kernel is launched with programmatic
+ * stream serialization, so it starts once every CTA of the kernel before it on the
+ * stream (the producer; the consumer in the serial schedule) is running, and works
+ * beside it. A token's sum waits on the device until its rows are final: the signal
+ * of each remote slot's (sender, destination) group and the ready flags of each
+ * local slot's row band; tokens whose slots are all remote go first. Any other work
+ * between the combine and this call on the stream (an event, a wait) makes it start
+ * after the combine instead, with the same results. Waits are bounded by timeout_ns
+ * (MOE_DEV_TIMEOUT); a status already set makes the kernel return. One call per
+ * moe_expert_combine (MOE_ERR_ARG otherwise). No CUDA events are recorded around it
+ * (they would keep it from overlapping); with moe_set_timing(plan, 2) the device clock
+ * records its span (moe_timings slots 7 and 8). */
+int moe_scale_gated(moe_plan *plan, const float *topk_w, const void *const *recv,
+                    void *const *out, moe_stream_t stream);
+
+/* Overlap of the combine copy with the expert FFN in the last moe_expert_combine made
+ * while device-clock records were on (moe_set_timing 1 or 2), the quantity of the TileMoE
+ * notes' section 7.3 (overlap ratio of the second all-to-all): *landed_frac is the share
+ * of the combine's bytes whose copies had landed when the producer finished its last
+ * output tile, *tail_us how long after that tile the last copy landed (negative if
+ * before), *copy_bytes the bytes copied. Synchronises the device. MOE_ERR_ARG if no
+ * such combine was recorded. Any output pointer may be NULL. */
+int moe_combine_overlap(moe_plan *plan, double *landed_frac, double *tail_us,
+                        double *copy_bytes);
+
 /* Plan build that allocates nothing, for callers that cannot call cudaMalloc (for
  * example a serving loop that reserved all of its device memory up front, or a
  * runtime whose device memory comes from an allocator it does not own). The pages
@@ -277,12 +306,15 @@ int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count)
  * recorded on the stream each kernel ran on: the mean over the calls made since
  * timing was last enabled (the most recent 64 of them). Synchronises on those
  * events. Order: [0] route (moe_route or moe_gate), [1] plan (all plan kernels and the gather),
- * [2] producer, [3] consumer, [4] scale, [5] gather only, and [6] the producer's
- * execution span on the device clock (its first CTA's start to its last CTA's end;
- * unlike [2] it excludes time spent queued behind other kernels, for example those
- * of another batch in flight). A slot with no measurement is -1. Instrumentation
- * only: events and spans are recorded only while enabled, and enabling resets the
- * counts. */
+ * [2] producer, [3] consumer, [4] scale, [5] gather only. Then, from the device clock,
+ * means over the last 64 combines: [6] the producer's execution span (its first CTA's
+ * start to its last CTA's end; unlike [2] it excludes time spent queued behind other
+ * kernels, for example those of another batch in flight), [7] the span of
+ * moe_scale_gated, [8] the part of [7] before the producer's end. A slot with no
+ * measurement is -1. Instrumentation only: moe_set_timing(plan, 1) records the events
+ * and the device-clock records, 2 only the device-clock records (no CUDA event enters
+ * the streams, so kernels keep overlapping as without timing), 0 nothing; enabling
+ * resets the counts. */
 int moe_set_timing(moe_plan *plan, int enable);
 int moe_timings(moe_plan *plan, float *ms, int n);
 

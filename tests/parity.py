@@ -97,15 +97,17 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().double().cpu().numpy()
 
 
-def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0, pairs=0, canaries=True):
+def run_gpu(wl, inp, mode="overlap", consumer_ctas=8, timeout_ns=0, pairs=0, canaries=True,
+            scale_mode="after"):
     """The whole path through the C ABI. mode: 'overlap' (two streams), 'serial', or
     'fused' (the copy inside the pair producer); pairs: 1 runs the CTA-pair producer
-    (0, the default here, keeps the one-CTA producer under test). With canaries the
+    (0, the default here, keeps the one-CTA producer under test); scale_mode "gated"
+    runs moe_scale_gated behind the combine instead of moe_scale. With canaries the
     receive and output buffers get guard rows and the rank workspaces start filled
     with the sentinel byte (check_canaries tests them after the run)."""
     cc = {"overlap": consumer_ctas, "serial": 0, "fused": -1}[mode]
     layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb,
-                          cc, timeout_ns, 1 if mode == "fused" else pairs)
+                          cc, timeout_ns, 1 if mode == "fused" else pairs, scale_mode=scale_mode)
     if canaries:
         install_canaries(layer)
     sp = torch.cuda.Stream()

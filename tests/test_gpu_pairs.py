@@ -129,3 +129,71 @@ def test_fused_device_wait_timeout_is_reported_and_recoverable():
     layer.close()
     layer = P.run_gpu(wl, inp, mode="fused")
     assert layer.status() == (0, 0)
+
+
+# ---------------------------------------------------------------- overlapped scale
+# moe_scale_gated: launched behind the combine, it starts beside the producer and
+# waits on the device for each token's group signals and ready flags.
+
+@pytest.mark.parametrize("mode", ["fused", "serial", "overlap"])
+@pytest.mark.parametrize("wl", [get_workload("tiny")] + SMALL, ids=lambda w: w.name)
+def test_gated_scale_equals_scale_after(wl, mode):
+    """Bit-identical outputs to the scale after the combine, and the complete oracle
+    check, for every schedule of the combine (in the two-stream schedule nothing
+    overlaps: the producer stream waits for the consumer before the scale)."""
+    inp = P.inputs_for(wl)
+    after = P.run_gpu(wl, inp, mode=mode, consumer_ctas=4, pairs=1)
+    gated = P.run_gpu(wl, inp, mode=mode, consumer_ctas=4, pairs=1, scale_mode="gated")
+    assert after.status() == (0, 0) and gated.status() == (0, 0)
+    for a, b in zip(after.out, gated.out):
+        assert torch.equal(a, b)
+    orc = P.oracle_run(wl, inp)
+    P.check_layout_and_outputs(gated, wl, inp, orc)
+    after.close()
+    gated.close()
+
+
+def test_gated_scale_once_per_combine():
+    wl = get_workload("tiny")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="fused", scale_mode="gated")
+    assert layer.status() == (0, 0)
+    with pytest.raises(capi.MoeError, match="MOE_ERR_ARG"):
+        layer.scale_gated()  # no combine since the last one
+    layer.close()
+
+
+def test_device_clock_records_of_an_overlapped_step():
+    """Timing mode 2 (device clock only): the producer's span, the overlapped scale's
+    span and its part before the producer's end, and the combine's overlap record: the
+    bytes copied are exactly the remote rows, a share of them landed before the last
+    tile, and the last copy landed within the step."""
+    wl = get_workload("qwen3_235b_like")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="fused", scale_mode="gated", canaries=False)
+    layer.set_timing(2)
+    sp = torch.cuda.Stream()
+    for _ in range(3):
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                      producer=sp)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    t = layer.timings()
+    assert all(v == -1 for v in t[:6]), "no CUDA events in mode 2"
+    assert t[6] > 0 and t[7] > 0 and 0 <= t[8] <= t[7] + 1e-3, t
+    landed, tail_us, nbytes = layer.combine_overlap()
+    recv_rows = int(layer.field(capi.MOE_PLAN_RECV_ROWS).sum())
+    assert nbytes == 2.0 * wl.d_model * recv_rows
+    assert 0.0 <= landed <= 1.0 and tail_us < 1e3 * t[6], (landed, tail_us)
+    layer.close()
+
+
+def test_gated_scale_device_wait_timeout_is_reported_and_recoverable():
+    wl = get_workload("a100_like")
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="fused", timeout_ns=20_000, scale_mode="gated")
+    code, _ = layer.status()
+    assert code == capi.MOE_DEV_TIMEOUT
+    layer.close()
+    layer = P.run_gpu(wl, inp, mode="fused", scale_mode="gated")
+    assert layer.status() == (0, 0)

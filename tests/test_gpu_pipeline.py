@@ -13,16 +13,17 @@ from tile_signaled_grouped_gb300.runtime import ExpertCombine, HostPipeline  # n
 from tile_signaled_grouped_gb300.workloads import get_workload, make_inputs  # noqa: E402
 
 
-@pytest.mark.parametrize("n_layers,cctas", [(1, 4), (2, 4), (2, -1)])
+@pytest.mark.parametrize("n_layers,cctas,scale", [(1, 4, "after"), (2, 4, "after"),
+                                                  (2, -1, "after"), (2, -1, "gated")])
 @pytest.mark.parametrize("name", ["tiny", "a100_like"])
-def test_pipelined_steps_equal_plain_forward(name, n_layers, cctas):
+def test_pipelined_steps_equal_plain_forward(name, n_layers, cctas, scale):
     base = get_workload(name)
     sets = [make_inputs(get_workload(name, seed=s), device="cuda", with_weights=s == 0)
             for s in (0, 3, 5)]
     w = sets[0]  # one set of expert weights for every step
     torch.cuda.synchronize()  # inputs are drawn on the default stream; the layer runs on others
     mk = lambda: ExpertCombine(base.W, base.L, base.topk, base.T, base.d_model, base.d_ff,
-                               base.tb_M, base.mgb, consumer_ctas=cctas)
+                               base.tb_M, base.mgb, consumer_ctas=cctas, scale_mode=scale)
     ref_layer = mk()
     sp, sc = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
     want = []
@@ -128,25 +129,26 @@ def test_tuned_schedule_keeps_results_exact():
         layer.set_schedule(4, 0)
 
 
-@pytest.mark.parametrize("cctas", [-1, 4])
-def test_captured_graph_replays_exactly(cctas):
+@pytest.mark.parametrize("cctas,scale", [(-1, "after"), (4, "after"), (-1, "gated")])
+def test_captured_graph_replays_exactly(cctas, scale):
     """A whole step captured into a CUDA graph (fused, or producer and consumer on two
-    streams joined by events) and replayed with new inputs written into the captured
-    tensors gives, replay by replay, exactly the eager step's outputs."""
+    streams joined by events; the overlapped scale becomes a programmatic edge) and
+    replayed with new inputs written into the captured tensors gives, replay by replay,
+    exactly the eager step's outputs."""
     name = "tiny"
     base = get_workload(name)
     sets = [make_inputs(get_workload(name, seed=s), device="cuda") for s in (0, 4)]
     w = sets[0]
     torch.cuda.synchronize()
     eager = ExpertCombine(base.W, base.L, base.topk, base.T, base.d_model, base.d_ff, base.tb_M,
-                          base.mgb, consumer_ctas=cctas)
+                          base.mgb, consumer_ctas=cctas, scale_mode=scale)
     want = []
     for inp in sets:
         out = eager.forward(inp.x, w.w_gate, w.w_up, w.w_down, inp.logits, inp.forced_ids)
         torch.cuda.synchronize()
         want.append([t.clone() for t in out])
     layer = ExpertCombine(base.W, base.L, base.topk, base.T, base.d_model, base.d_ff, base.tb_M,
-                          base.mgb, consumer_ctas=cctas)
+                          base.mgb, consumer_ctas=cctas, scale_mode=scale)
     x = [t.clone() for t in sets[0].x]
     logits = sets[0].logits.clone()
     graph = layer.capture(x, w.w_gate, w.w_up, w.w_down, logits)

@@ -81,6 +81,9 @@ def load():
         "moe_plan_build": (ip, [vp, vp, P(vp), vp]),
         "moe_expert_combine": (ip, [vp, P(vp), P(vp), P(vp), P(vp), vp, vp]),
         "moe_scale": (ip, [vp, vp, P(vp), P(vp), vp]),
+        "moe_scale_gated": (ip, [vp, vp, P(vp), P(vp), vp]),
+        "moe_combine_overlap": (ip, [vp, P(ctypes.c_double), P(ctypes.c_double),
+                                     P(ctypes.c_double)]),
         "moe_status": (ip, [vp, vp, P(ip), P(ip)]),
         "moe_status_clear": (ip, [vp, vp]),
         "moe_field": (ip, [P(moe_cfg), ip, P(sz), P(sz)]),
@@ -169,6 +172,18 @@ def moe_scale(plan, topk_w, recv, out, stream):
     check(lib().moe_scale(plan, topk_w, ptr_array(recv), ptr_array(out), stream), "moe_scale")
 
 
+def moe_scale_gated(plan, topk_w, recv, out, stream):
+    check(lib().moe_scale_gated(plan, topk_w, ptr_array(recv), ptr_array(out), stream),
+          "moe_scale_gated")
+
+
+def moe_combine_overlap(plan):
+    """(landed_frac, tail_us, copy_bytes) of the last recorded combine."""
+    v = [ctypes.c_double() for _ in range(3)]
+    check(lib().moe_combine_overlap(plan, *[ctypes.byref(x) for x in v]), "moe_combine_overlap")
+    return tuple(x.value for x in v)
+
+
 def moe_status(plan, stream):
     code, detail = ctypes.c_int(), ctypes.c_int()
     check(lib().moe_status(plan, stream, ctypes.byref(code), ctypes.byref(detail)), "moe_status")
@@ -179,8 +194,9 @@ def moe_status_clear(plan, stream):
     check(lib().moe_status_clear(plan, stream), "moe_status_clear")
 
 
-def moe_set_timing(plan, enable: bool):
-    check(lib().moe_set_timing(plan, int(bool(enable))), "moe_set_timing")
+def moe_set_timing(plan, mode):
+    """mode: 0/False off, 1/True CUDA events and device-clock records, 2 device clock only."""
+    check(lib().moe_set_timing(plan, int(mode)), "moe_set_timing")
 
 
 def moe_timings(plan, n: int = 6):

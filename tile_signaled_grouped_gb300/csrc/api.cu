@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -39,9 +40,12 @@ struct moe_plan {
   cudaEvent_t ev_ready, ev_join;
   cudaEvent_t ev_t0[kTSlots][kTRing], ev_t1[kTSlots][kTRing];
   int nrec[kTSlots];  // measurements recorded since timing was enabled
-  int nspan;          // producer kernel spans recorded since timing was enabled
+  int nspan;          // combines whose device-clock records were kept since timing was enabled
+  int last_span;      // ring record of the last combine (-1: none)
   bool xprev_ready;   // PA_XPREV holds the rows' contents (set by the first plan build)
-  bool timing;
+  bool timing;        // CUDA events around each kernel
+  bool spans;         // device-clock records (span ring, chunk landing stamps)
+  bool gated_armed;   // a combine was enqueued since the last moe_scale_gated
 };
 
 namespace moe {
@@ -122,8 +126,11 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_SCALE_SRC] = W * (size_t)d.T * d.k;
   n[PA_PAIR] = 4 * W * NMM;
   n[PA_PAIR_UNIT_BEGIN] = n[PA_UNIT_BEGIN];
-  n[PA_SPANS] = 4 * kSpanRing;
+  n[PA_SPANS] = 2 * kSpanWords * kSpanRing;
   n[PA_XPREV] = W * (size_t)d.RM;
+  // Copy chunks of one combine: at most one partial chunk per segment beyond the
+  // remote rows (at most W * T * topk) cut into chunks of rpc rows.
+  n[PA_CHUNK_T] = 2 * (W * (size_t)d.T * d.k / d.rpc + W * NBM + 1);
   size_t pos = 0;
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;
@@ -162,7 +169,14 @@ DevPlan dev_plan(const moe_plan* p) {
   for (int i = 0; i < PA_COUNT; ++i)
     dp.a[i] = reinterpret_cast<int32_t*>(p->plan_ws + p->offsets[i]);
   dp.timeout_ns = p->cfg.timeout_ns > 0 ? p->cfg.timeout_ns : 2000000000LL;
+  dp.span = nullptr;
+  dp.chunk_t = nullptr;
   return dp;
+}
+
+unsigned long long* span_record(const moe_plan* p, int slot) {
+  return reinterpret_cast<unsigned long long*>(p->plan_ws + p->offsets[PA_SPANS]) +
+         (size_t)kSpanWords * (slot % kSpanRing);
 }
 
 struct LaunchShape {
@@ -294,6 +308,7 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
   if (p == nullptr) return MOE_ERR_ARG;
   p->cfg = *cfg;
   p->d = d;
+  p->last_span = -1;
   p->plan_ws = static_cast<uint8_t*>(plan_ws);
   for (int r = 0; r < d.W; ++r) p->rank_ws[r] = static_cast<uint8_t*>(rank_ws[r]);
   std::memcpy(p->offsets, off, sizeof(off));
@@ -428,11 +443,11 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
   ProducerArgs pa;
   std::memset(&pa, 0, sizeof(pa));
   pa.p = dev_plan(p);
-  if (p->timing) {  // the producer folds its execution span into a zeroed ring slot
-    unsigned long long* ring =
-        reinterpret_cast<unsigned long long*>(p->plan_ws + p->offsets[PA_SPANS]);
-    pa.span = ring + 2 * (p->nspan % kSpanRing);
-    CUDA_TRY(cudaMemsetAsync(pa.span, 0, 2 * sizeof(unsigned long long), sp));
+  if (p->spans) {  // the kernels fold their device-clock stamps into a zeroed ring record
+    pa.p.span = span_record(p, p->nspan);
+    pa.p.chunk_t = reinterpret_cast<unsigned long long*>(p->plan_ws + p->offsets[PA_CHUNK_T]);
+    CUDA_TRY(cudaMemsetAsync(pa.p.span, 0, kSpanWords * sizeof(unsigned long long), sp));
+    p->last_span = p->nspan % kSpanRing;
     p->nspan++;
   }
   for (int r = 0; r < d.W; ++r) {
@@ -465,10 +480,12 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
     ca.recv[r] = static_cast<__nv_bfloat16*>(recv[r]);
   }
 
-  // Ready flags, GEMM1 counters, the ticket counter and the group signals start at 0.
+  // Ready flags, GEMM1 counters, the ticket counters (the producer's and the overlapped
+  // scale's) and the group signals start at 0.
   const size_t z0 = p->offsets[PA_QUEUE];
   const size_t z1 = p->offsets[PA_GROUP_SIG] + p->counts[PA_GROUP_SIG] * 4;
   CUDA_TRY(cudaMemsetAsync(p->plan_ws + z0, 0, z1 - z0, sp));
+  p->gated_armed = true;
   if (fused) {
     tstart(p, kTProducer, sp);
     CUDA_TRY(launch_producer_pair(pa, pgrid, true, sp));
@@ -516,6 +533,74 @@ int moe_scale(moe_plan* p, const float* topk_w, const void* const* recv, void* c
   return MOE_OK;
 }
 
+int moe_scale_gated(moe_plan* p, const float* topk_w, const void* const* recv, void* const* out,
+                    moe_stream_t stream) {
+  if (p == nullptr || !aligned16(topk_w) || recv == nullptr || out == nullptr || !p->gated_armed)
+    return MOE_ERR_ARG;
+  const Dims& d = p->d;
+  ScaleArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = dev_plan(p);
+  a.w = topk_w;
+  for (int r = 0; r < d.W; ++r) {
+    if (!aligned16(recv[r]) || !aligned16(out[r])) return MOE_ERR_ARG;
+    a.recv[r] = static_cast<const __nv_bfloat16*>(recv[r]);
+    a.y[r] = reinterpret_cast<const __nv_bfloat16*>(p->rank_ws[r] + p->rl.y_off);
+    a.out[r] = static_cast<__nv_bfloat16*>(out[r]);
+  }
+  if (p->spans && p->last_span >= 0) a.p.span = span_record(p, p->last_span);
+  // No CUDA events around this launch: an event between the previous kernel and this
+  // one would keep the launch from starting beside it.
+  CUDA_TRY(launch_scale_gated(a, p->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  p->gated_armed = false;
+  return MOE_OK;
+}
+
+int moe_combine_overlap(moe_plan* p, double* landed_frac, double* tail_us, double* copy_bytes) {
+  if (p == nullptr || !p->spans || p->last_span < 0) return MOE_ERR_ARG;
+  CUDA_TRY(cudaDeviceSynchronize());
+  unsigned long long rec[kSpanWords];
+  CUDA_TRY(cudaMemcpy(rec, span_record(p, p->last_span), sizeof(rec), cudaMemcpyDeviceToHost));
+  int32_t tot[8];
+  CUDA_TRY(cudaMemcpy(tot, p->plan_ws + p->offsets[PA_TOTALS], sizeof(tot), cudaMemcpyDeviceToHost));
+  const int nseg = tot[1], nch = tot[4];
+  double total = 0.0, before = 0.0;
+  long long tail = LLONG_MIN;
+  if (nseg > 0 && nch > 0) {
+    int32_t* recs = new (std::nothrow) int32_t[(size_t)nseg * kSegRec];
+    unsigned long long* st = new (std::nothrow) unsigned long long[nch];
+    if (recs == nullptr || st == nullptr) {
+      delete[] recs;
+      delete[] st;
+      return MOE_ERR_ARG;
+    }
+    cudaError_t e = cudaMemcpy(recs, p->plan_ws + p->offsets[PA_SEG_REC],
+                               (size_t)nseg * kSegRec * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(st, p->plan_ws + p->offsets[PA_CHUNK_T], (size_t)nch * 8,
+                     cudaMemcpyDeviceToHost);
+    const unsigned long long last_tile = rec[kSpanLastTile];
+    for (int i = 0; e == cudaSuccess && i < nseg; ++i) {
+      const int32_t* r = recs + (size_t)i * kSegRec;
+      for (int k = 0; k < r[7]; ++k) {
+        const int rows = std::min(p->d.rpc, r[4] - k * p->d.rpc);
+        const double bytes = (double)rows * p->d.D * 2.0;
+        const unsigned long long t = st[r[6] + k];
+        total += bytes;
+        if (t <= last_tile) before += bytes;
+        tail = std::max(tail, (long long)(t - last_tile));
+      }
+    }
+    delete[] recs;
+    delete[] st;
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (landed_frac) *landed_frac = total > 0.0 ? before / total : 1.0;
+  if (tail_us) *tail_us = tail == LLONG_MIN ? 0.0 : (double)tail * 1e-3;
+  if (copy_bytes) *copy_bytes = total;
+  return MOE_OK;
+}
+
 int moe_set_schedule(moe_plan* p, int consumer_ctas, int mgb) {
   if (p == nullptr) return MOE_ERR_ARG;
   moe_cfg c = p->cfg;
@@ -559,10 +644,12 @@ int moe_status_clear(moe_plan* p, moe_stream_t stream) {
 }
 
 int moe_set_timing(moe_plan* p, int enable) {
-  if (p == nullptr) return MOE_ERR_ARG;
-  p->timing = enable != 0;
+  if (p == nullptr || enable < 0 || enable > 2) return MOE_ERR_ARG;
+  p->timing = enable == 1;
+  p->spans = enable != 0;
   for (int i = 0; i < kTSlots; ++i) p->nrec[i] = 0;
   p->nspan = 0;
+  p->last_span = -1;
   return MOE_OK;
 }
 
@@ -582,21 +669,31 @@ int moe_timings(moe_plan* p, float* ms, int n) {
     }
     ms[i] = (float)(sum / m);
   }
-  if (n > kTSlots) {  // producer kernel span on the device clock
-    ms[kTSlots] = -1.f;
-    const int m = std::min(p->nspan, kSpanRing);
-    if (m > 0) {
-      CUDA_TRY(cudaDeviceSynchronize());
-      unsigned long long ring[2 * kSpanRing];
-      CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
-                          cudaMemcpyDeviceToHost));
-      double sum = 0.0;
-      for (int j = 0; j < m; ++j) {
-        const int q = (p->nspan - 1 - j) % kSpanRing;
-        sum += (double)(ring[2 * q + 1] - ~ring[2 * q]) * 1e-6;
+  // Device-clock records: [6] the producer's span, [7] the overlapped scale's span,
+  // [8] the part of that span before the producer's end (means over the records).
+  for (int i = kTSlots; i < n && i < kTSlots + 3; ++i) ms[i] = -1.f;
+  const int m = std::min(p->nspan, kSpanRing);
+  if (n > kTSlots && m > 0) {
+    CUDA_TRY(cudaDeviceSynchronize());
+    unsigned long long ring[kSpanWords * kSpanRing];
+    CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
+                        cudaMemcpyDeviceToHost));
+    double prod = 0.0, scale = 0.0, beside = 0.0;
+    int nscale = 0;
+    for (int j = 0; j < m; ++j) {
+      const unsigned long long* r = ring + (size_t)kSpanWords * ((p->nspan - 1 - j) % kSpanRing);
+      const unsigned long long p0 = ~r[kSpanProdStart], p1 = r[kSpanProdEnd];
+      prod += (double)(p1 - p0) * 1e-6;
+      if (r[kSpanScaleStart] != 0) {
+        const unsigned long long s0 = ~r[kSpanScaleStart], s1 = r[kSpanScaleEnd];
+        scale += (double)(s1 - s0) * 1e-6;
+        beside += s0 < p1 ? (double)(std::min(s1, p1) - s0) * 1e-6 : 0.0;
+        ++nscale;
       }
-      ms[kTSlots] = (float)(sum / m);
     }
+    ms[kTSlots] = (float)(prod / m);
+    if (nscale > 0 && n > kTSlots + 1) ms[kTSlots + 1] = (float)(scale / nscale);
+    if (nscale > 0 && n > kTSlots + 2) ms[kTSlots + 2] = (float)(beside / nscale);
   }
   return MOE_OK;
 }

@@ -69,6 +69,7 @@ __device__ __forceinline__ void combine_copy(const DevPlan& p, const __nv_bfloat
   };
   Pend pend[kChunkSlots] = {};
   int n = 0, stored = 0;
+  int released = 0;         // lane 0: chunks released (their landing stamped) so far
   bool unreleased = false;  // lane 0: chunks stored since the last release
   bool ok = true;
   const long long itimeout = p.timeout_ns + 4000000000LL;
@@ -100,6 +101,13 @@ __device__ __forceinline__ void combine_copy(const DevPlan& p, const __nv_bfloat
       fence_proxy_async_global();
       fence_acq_rel_gpu();
       unreleased = false;
+      if (p.chunk_t != nullptr) {
+        // Timing on: every chunk stored since the last release has landed by now.
+        // This CTA's m-th chunk is chunk c + m * G of the global sequence.
+        const unsigned long long now = globaltimer();
+        for (int m = released; m < stored; ++m) p.chunk_t[c + (size_t)m * G] = now;
+      }
+      released = stored;
     }
     __syncwarp();
     for (int g = lane; g < kMaxGroups; g += 32) {

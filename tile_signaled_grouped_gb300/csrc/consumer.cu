@@ -32,6 +32,7 @@ static_assert(sizeof(ConsumerSmem) <= kConsumerSmemTail, "consumer shared memory
 __global__ void __launch_bounds__(kConsumerThreads, 1)
     consumer_kernel(const __grid_constant__ ConsumerArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  allow_dependent_launch();  // a scale launched behind this kernel may start beside it
   ConsumerSmem& sm =
       *reinterpret_cast<ConsumerSmem*>(smem_raw + (size_t)kChunkSlots * kChunkBytes);
   combine_copy<kChunkSlots, kLoadsInFlight, 8>(a.p, a.y, a.recv, smem_raw, sm, blockIdx.x,

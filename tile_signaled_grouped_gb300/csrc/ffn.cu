@@ -119,6 +119,7 @@ __device__ Task decode_ticket(const Smem& sm, const ProducerArgs& a, long long t
 __global__ void __launch_bounds__(kProducerThreads, 1)
     ffn_producer_kernel(const __grid_constant__ ProducerArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  allow_dependent_launch();  // a scale launched behind this kernel may start beside it
   const Dims d = a.p.d;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
-  if (threadIdx.x == 0) span_begin(a.span);
+  if (threadIdx.x == 0) span_begin(a.p.span);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
           const int last = min(tk.row0 + kTileM, rows_lim) - 1;
           for (int b = tk.row0 / d.tb; b <= last / d.tb; ++b)
             red_release_add_u32(flags + ((size_t)tk.o * d.NBM + b) * d.nt2 + tk.nt, 1u);
+          span_end(a.p.span, kSpanLastTile);
         }
       }
     }
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
     __syncwarp();
     tmem_dealloc(tmem_base, 2 * kAccCols);
   }
-  if (threadIdx.x == 0) span_end(a.span);
+  if (threadIdx.x == 0) span_end(a.p.span);
 }
 
 }  // namespace

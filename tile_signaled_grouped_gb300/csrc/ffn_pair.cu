@@ -238,6 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
     ffn_pair_kernel(const __grid_constant__ ProducerArgs a) {
   constexpr int kPStages = PairCfg<FUSED>::kStages;
   extern __shared__ uint8_t smem_raw[];
+  allow_dependent_launch();  // a scale launched behind this kernel may start beside it
   const Dims d = a.p.d;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -295,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
   cluster_sync_all();  // both CTAs: barriers initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
-  if (threadIdx.x == 0) span_begin(a.span);
+  if (threadIdx.x == 0) span_begin(a.p.span);
 
   if (FUSED && warp == kCopyWarp) {
     // ------------------------------------------------------------ combine copy
@@ -554,6 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
             const int last = min(tk.row0 + kTileM, rows_lim) - 1;
             for (int b = tk.row0 / d.tb; b <= last / d.tb; ++b)
               red_release_add_u32(flags + ((size_t)tk.o * d.NBM + b) * d.nt2 + tk.nt, 1u);
+            span_end(a.p.span, kSpanLastTile);
           }
         }
       }
@@ -571,7 +573,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
     __syncwarp();
     tmem_dealloc_pair(tmem_base, 2 * kPAccCols);
   }
-  if (threadIdx.x == 0) span_end(a.span);
+  if (threadIdx.x == 0) span_end(a.p.span);
 }
 
 }  // namespace

@@ -30,7 +30,16 @@ constexpr size_t kConsumerSmemTail = 12 * 1024;  // barriers, counters and recor
 constexpr size_t kConsumerSmem = (size_t)kChunkSlots * kChunkBytes + kConsumerSmemTail;
 constexpr int kSegRec = 8;                   // ints per consumer segment record
 constexpr int kMaxSegChunks = 256;           // copy chunks one segment may have
-constexpr int kSpanRing = 64;                // producer kernel spans kept while timing
+constexpr int kSpanRing = 64;                // per-combine device-clock records kept while timing
+// One record of the span ring: eight u64 device-clock stamps (ns) of one combine.
+enum SpanWord {
+  kSpanProdStart = 0,   // ~(first producer CTA start), folded in with atomicMax
+  kSpanProdEnd = 1,     // last producer CTA end
+  kSpanScaleStart = 2,  // ~(first CTA start) of the overlapped scale
+  kSpanScaleEnd = 3,    // last CTA end of the overlapped scale
+  kSpanLastTile = 4,    // the producer's last finished output tile (its ready-flag release)
+  kSpanWords = 8
+};
 
 // ---------------------------------------------------------------------------
 // Dimensions derived from a configuration (host and device).
@@ -65,8 +74,9 @@ enum PlanArray {
   PA_SEG_REC, PA_GROUP_NCHUNK,
   PA_XSRC, PA_SCALE_SRC,
   PA_PAIR, PA_PAIR_UNIT_BEGIN,
-  PA_SPANS,  // [kSpanRing][2] u64: producer kernel spans recorded while timing is on
+  PA_SPANS,  // [kSpanRing][kSpanWords] u64: device-clock records of each combine while timing
   PA_XPREV,  // [W][RM] what each X row held after the last gather: token, -1 zero, else unknown
+  PA_CHUNK_T,  // [chunks] u64: device clock when each copy chunk had landed (timing on)
   PA_COUNT
 };
 
@@ -90,6 +100,10 @@ struct DevPlan {
   Dims d;
   int32_t* a[PA_COUNT];
   long long timeout_ns;
+  // Timing on: this combine's record of the span ring (kSpanWords u64, zeroed by the
+  // host) and the chunk landing stamps; both null otherwise.
+  unsigned long long* span;
+  unsigned long long* chunk_t;
 };
 
 // ---------------------------------------------------------------------------
@@ -137,9 +151,6 @@ struct ProducerArgs {
   __nv_bfloat16* h[MOE_MAX_RANKS];
   __nv_bfloat16* y[MOE_MAX_RANKS];
   __nv_bfloat16* recv[MOE_MAX_RANKS];  // receive buffers (the fused pair producer copies into them)
-  // Timing on: the kernel's execution span on the device clock, {~first CTA start,
-  // last CTA end}, both folded in with atomicMax into a slot the host zeroed.
-  unsigned long long* span;
   DevPlan p;
   int lag;  // scheduling units between a unit's GEMM1 tiles and its GEMM2 tiles
 };
@@ -167,6 +178,9 @@ struct ScaleArgs {
   DevPlan p;
 };
 cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s);
+// The scale overlapped with the kernel before it on the stream (a programmatic
+// dependent launch): its per-token waits on group signals and ready flags.
+cudaError_t launch_scale_gated(const ScaleArgs& a, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Device helpers.
@@ -179,12 +193,20 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-// Producer kernel span (timing on): the first CTA's start and the last CTA's end.
-__device__ __forceinline__ void span_begin(unsigned long long* span) {
-  if (span != nullptr) atomicMax(span, ~globaltimer());
+// A kernel's span (timing on): the first CTA's start (stored complemented, so that
+// atomicMax keeps the earliest) and the last CTA's end, in the combine's span record.
+__device__ __forceinline__ void span_begin(unsigned long long* span, int word = kSpanProdStart) {
+  if (span != nullptr) atomicMax(span + word, ~globaltimer());
 }
-__device__ __forceinline__ void span_end(unsigned long long* span) {
-  if (span != nullptr) atomicMax(span + 1, globaltimer());
+__device__ __forceinline__ void span_end(unsigned long long* span, int word = kSpanProdEnd) {
+  if (span != nullptr) atomicMax(span + word, globaltimer());
+}
+
+// Lets the kernel launched after this one on the stream with programmatic stream
+// serialization start once every CTA of this grid has executed it (or exited); that
+// kernel synchronises with this one only through device-memory flags.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // First error wins; detail is written by the same winner.

@@ -22,9 +22,15 @@ class ExpertCombine:
 
     def __init__(self, W, L, topk, T, d_model, d_ff, tb_M, mgb=1,
                  consumer_ctas=capi.MOE_CONSUMER_FUSED, timeout_ns=0, producer_pairs=1,
-                 device=None):
+                 device=None, scale_mode="after"):
         """consumer_ctas: MOE_CONSUMER_FUSED (-1, the copy runs in a warp of every pair
-        producer CTA), 0 (serial), or the consumer CTAs beside the producer."""
+        producer CTA), 0 (serial), or the consumer CTAs beside the producer.
+        scale_mode: "after" (moe_scale once the combine is done) or "gated"
+        (moe_scale_gated: the scale starts beside the producer and waits on the device
+        for each token's group signals and ready flags)."""
+        if scale_mode not in ("after", "gated"):
+            raise ValueError(f"scale_mode {scale_mode!r}")
+        self.scale_mode = scale_mode
         self.device = torch.device(device or "cuda")
         self.cfg = capi.moe_cfg(W, L, topk, T, d_model, d_ff, tb_M, mgb, consumer_ctas,
                                 timeout_ns, producer_pairs)
@@ -100,6 +106,21 @@ class ExpertCombine:
                        [t.data_ptr() for t in out], _stream_handle(stream))
         return out
 
+    def scale_gated(self, w=None, stream=None, out=None):
+        """The scale overlapped with the combine just enqueued on `stream` (its producer
+        stream): same results as scale()."""
+        w = self.w if w is None else w
+        out = self.out if out is None else out
+        capi.moe_scale_gated(self.plan, w.data_ptr(), [t.data_ptr() for t in self.recv],
+                             [t.data_ptr() for t in out], _stream_handle(stream))
+        return out
+
+    def scale_step(self, stream=None, out=None):
+        """The scale of a step, in the layer's scale_mode."""
+        if self.scale_mode == "gated":
+            return self.scale_gated(stream=stream, out=out)
+        return self.scale(stream=stream, out=out)
+
     def forward(self, x, w_gate, w_up, w_down, logits=None, forced_ids=None, producer=None,
                 consumer=None, out=None, w_router=None):
         """route -> plan -> overlapped FFN and combine -> scale; all on the GPU.
@@ -116,7 +137,7 @@ class ExpertCombine:
             self.route(logits, forced_ids, producer)
         self.plan_build(x, stream=producer)
         self.expert_combine(w_gate, w_up, w_down, producer, consumer)
-        return self.scale(stream=producer, out=out)
+        return self.scale_step(stream=producer, out=out)
 
     def capture(self, x, w_gate, w_up, w_down, logits=None, forced_ids=None, producer=None,
                 consumer=None, out=None, w_router=None):
@@ -195,11 +216,19 @@ class ExpertCombine:
         return capi.moe_launch_info(self.plan)
 
     def set_timing(self, enable=True):
+        """True/1: CUDA events and device-clock records; 2: device-clock records only
+        (nothing enters the streams); False/0: off."""
         capi.moe_set_timing(self.plan, enable)
 
     def timings(self):
-        """[route or gate, plan, producer, consumer, scale, gather, producer span] in ms (-1: none)."""
-        return capi.moe_timings(self.plan, 7)
+        """[route or gate, plan, producer, consumer, scale, gather, producer span,
+        gated-scale span, gated-scale time before the producer's end] in ms (-1: none)."""
+        return capi.moe_timings(self.plan, 9)
+
+    def combine_overlap(self):
+        """(share of the combine's bytes landed before the producer's last tile, µs from
+        that tile to the last copy, bytes copied) of the last combine recorded."""
+        return capi.moe_combine_overlap(self.plan)
 
 
 class HostPipeline:
@@ -281,10 +310,12 @@ class HostPipeline:
             lay.route(self.logits[b], fid, sp)
         lay.plan_build(self.x[b], stream=sp)
         self.ev_free[b].record(sp)
-        lay.expert_combine(w_gate, w_up, w_down, sp, sc)
+        # The output set is rewritten only after its previous copy to the host; the wait
+        # comes before the combine, so nothing separates the combine from the scale.
         if self.started[b]:
             sp.wait_event(self.ev_out[b])
-        lay.scale(stream=sp, out=self.out[b])
+        lay.expert_combine(w_gate, w_up, w_down, sp, sc)
+        lay.scale_step(stream=sp, out=self.out[b])
         self.ev_done[b].record(sp)
         self.s_out.wait_event(self.ev_done[b])
         with torch.cuda.stream(self.s_out):
