@@ -468,59 +468,50 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
             ser.setdefault(name, []).append(t[i])
     ser = {n: statistics.median(v) for n, v in ser.items()}
     del flush
-    # Consumer CTAs beside the producer: whole-step time for a few partitions.
-    sweep = {}
+    # Whole-step time of each schedule: consumer CTAs beside the producer (-1 fused,
+    # 0 serial, n CTAs), and the scale after the combine or overlapped with it
+    # (moe_scale_gated) with one batch at a time or two in flight. The GPU's clocks
+    # drift as it settles at its power cap, so the configurations take turns: rounds
+    # of a few steps each, the median over the rounds.
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for cc in [c for c in args.ccta_sweep if c >= -1]:
-        lay = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, cc,
-                            producer_pairs=args.producer_pairs)
-        for _ in range(3):
-            lay.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
-                        producer=sp, consumer=sc)
-        torch.cuda.synchronize()
-        ev0.record(sp)
-        for _ in range(iters * 4):
-            lay.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
-                        producer=sp, consumer=sc)
-        ev1.record(sp)
-        torch.cuda.synchronize()
-        sweep[str(cc)] = ev0.elapsed_time(ev1) / (iters * 4)
-        lay.close()
-        del lay
-    # Scale after the combine or overlapped with it (moe_scale_gated), with one batch at
-    # a time or two in flight: whole-step time of each.
-    scale_sweep = {}
-    for n_fly in (1, 2):
-        for mode in ("after", "gated"):
-            lays = [ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, args.consumer_ctas,
-                                  producer_pairs=args.producer_pairs, scale_mode=mode)
-                    for _ in range(n_fly)]
-            sps = [sp] + [torch.cuda.Stream() for _ in range(n_fly - 1)]
-            scs = [sc] + [torch.cuda.Stream(priority=-1) for _ in range(n_fly - 1)]
+    pair = [ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, -1,
+                          producer_pairs=args.producer_pairs) for _ in range(2)]
+    sps = [sp, torch.cuda.Stream()]
+    scs = [sc, torch.cuda.Stream(priority=-1)]
+    configs = [("cc", c, "after", 1) for c in args.ccta_sweep if c >= -1] + \
+              [("scale", args.consumer_ctas, m, n) for n in (1, 2) for m in ("after", "gated")]
+    times = {c: [] for c in configs}
+    for _round in range(4):
+        for cfg in configs:
+            kind, cc, mode, n_fly = cfg
+            for lay in pair:
+                lay.set_schedule(cc, wl.mgb)
+                lay.scale_mode = mode
 
             def run(i):
-                lays[i % n_fly].forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits,
-                                        inp.forced_ids, producer=sps[i % n_fly],
-                                        consumer=scs[i % n_fly])
+                j = i % n_fly
+                pair[j].forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits,
+                                inp.forced_ids, producer=sps[j], consumer=scs[j])
 
-            for i in range(3 * n_fly):
+            for i in range(2 * n_fly):
                 run(i)
             torch.cuda.synchronize()
             ev0.record(sp)
-            for s_ in sps[1:]:
-                s_.wait_event(ev0)
-            for i in range(iters * 4):
+            sps[1].wait_event(ev0)
+            for i in range(iters):
                 run(i)
-            for s_ in sps[1:]:
-                sp.wait_stream(s_)
+            sp.wait_stream(sps[1])
             ev1.record(sp)
             torch.cuda.synchronize()
-            for lay in lays:
-                if lay.status() != (0, 0):
-                    raise RuntimeError(f"device status {lay.status()} in the scale sweep")
-                lay.close()
-            scale_sweep[f"{mode}_x{n_fly}"] = ev0.elapsed_time(ev1) / (iters * 4)
-            del lays
+            times[cfg].append(ev0.elapsed_time(ev1) / iters)
+    for lay in pair:
+        if lay.status() != (0, 0):
+            raise RuntimeError(f"device status {lay.status()} in the schedule sweep")
+        lay.close()
+    del pair
+    sweep = {str(c[1]): statistics.median(v) for c, v in times.items() if c[0] == "cc"}
+    scale_sweep = {f"{c[2]}_x{c[3]}": statistics.median(v) for c, v in times.items()
+                   if c[0] == "scale"}
     # The same step captured once into a CUDA graph and replayed (one host launch per step).
     layer.set_timing(False)
     graph = layer.capture(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
@@ -553,6 +544,8 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         "serial_ms": ser,
         "step_ms_by_consumer_ctas": sweep,
         "step_ms_by_scale_and_batches_in_flight": scale_sweep,
+        "schedule_sweep_timing": ("whole steps, CUDA events; 4 interleaved rounds of "
+                                  f"{iters} steps per configuration, median"),
         "step_ms_graph_replay": graph_ms,
         "producer_alone_tflops": flops / (ser["producer"] * 1e-3) / 1e12,
         "producer_alone_frac_burst": flops / (ser["producer"] * 1e-3) / 1e12 / bf16,

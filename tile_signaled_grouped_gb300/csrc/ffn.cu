@@ -381,7 +381,8 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
           const int last = min(tk.row0 + kTileM, rows_lim) - 1;
           for (int b = tk.row0 / d.tb; b <= last / d.tb; ++b)
             red_release_add_u32(flags + ((size_t)tk.o * d.NBM + b) * d.nt2 + tk.nt, 1u);
-          span_end(a.p.span, kSpanLastTile);
+          red_release_add_u32(queue + 3, 1u);  // output tiles finished (the scale's gate)
+            span_end(a.p.span, kSpanLastTile);
         }
       }
     }

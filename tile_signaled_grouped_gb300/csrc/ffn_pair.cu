@@ -555,6 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
             const int last = min(tk.row0 + kTileM, rows_lim) - 1;
             for (int b = tk.row0 / d.tb; b <= last / d.tb; ++b)
               red_release_add_u32(flags + ((size_t)tk.o * d.NBM + b) * d.nt2 + tk.nt, 1u);
+            red_release_add_u32(queue + 3, 1u);  // output tiles finished (the scale's gate)
             span_end(a.p.span, kSpanLastTile);
           }
         }

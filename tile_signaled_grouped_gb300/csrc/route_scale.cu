@@ -34,14 +34,14 @@ __global__ void __launch_bounds__(256) route_kernel(DevPlan p, const float* __re
                        ids + (size_t)tok * d.k, w + (size_t)tok * d.k, lane);
 }
 
-// One warp per token (s, t): out_s[t] = sum_j w_j * row_j, fp32 in slot order.
-// Lane j < k holds slot j's source (scale map) and weight; the next token's are
-// fetched while the current token is summed. Each lane covers two 16-byte chunks
-// of the row per pass and gathers up to four slots' chunks into registers before
-// accumulating, so a lane keeps up to eight independent 16-byte loads in flight.
-// Slot order of the fp32 sum is kept (j ascending).
-constexpr int kScaleGroup = 4;
-
+// Scale: out_s[t] = sum_j w_j * row_j, fp32 in slot order, bf16 out, by whole warps:
+// lane j < k holds slot j's source (scale map) and weight. A round covers 32 * CPL
+// 16-byte chunks of the output row (CPL per lane) and walks the slots in groups of SG,
+// loading a group's SG * CPL chunks per lane before accumulating, so every lane keeps
+// eight independent 16-byte loads in flight: SG = 4, CPL = 2 for k >= 4; SG = 2,
+// CPL = 4 for k < 4 (for k = 1 half of them; measured faster than SG = 1, CPL = 8, whose
+// 95 registers leave two CTAs per SM). Each element's sum is its k products added in
+// slot order (a group's unused slots add 0 * 0).
 __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -52,107 +52,86 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4
   }
 }
 
+// One round of token (s, t): chunks c0 + 32 i + lane, i < CPL. L2ONLY reads the rows
+// from L2 (__ldcg) for rows that a kernel still running beside this one has written
+// (the read-only and L1 paths are not kept coherent with such writes); otherwise
+// through the read-only path.
+template <int SG, int CPL, bool L2ONLY>
+__device__ __forceinline__ void scale_round(const ScaleArgs& a, const Dims& d, int s, int t,
+                                            int src_l, float w_l, int lane, int c0) {
+  const int n16 = d.D / 8;
+  float acc[CPL][8];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+  for (int j0 = 0; j0 < d.k; j0 += SG) {
+    uint4 v[SG][CPL];
+    float wj[SG];
+#pragma unroll
+    for (int q = 0; q < SG; ++q) {
+      const int j = j0 + q;
+      const int sj = __shfl_sync(0xffffffffu, src_l, j & 31);
+      wj[q] = __shfl_sync(0xffffffffu, w_l, j & 31);
+      // Slots past k, and invalid routing slots (reported by the plan), add nothing.
+      const bool live = j < d.k && sj != INT_MIN;
+      if (!live) wj[q] = 0.f;
+      const uint4* row = reinterpret_cast<const uint4*>(
+          sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D);
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = c0 + 32 * i + lane;
+        v[q][i] = !(live && c < n16) ? make_uint4(0, 0, 0, 0)
+                  : L2ONLY           ? __ldcg(row + c)
+                                     : __ldg(row + c);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < SG; ++q)
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) fma_bf16x8(acc[i], wj[q], v[q][i]);
+  }
+  uint4* out = reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = c0 + 32 * i + lane;
+    if (c < n16)
+      out[c] = make_uint4(pack_bf16x2(acc[i][0], acc[i][1]), pack_bf16x2(acc[i][2], acc[i][3]),
+                          pack_bf16x2(acc[i][4], acc[i][5]), pack_bf16x2(acc[i][6], acc[i][7]));
+  }
+}
+
+// After the combine. A task is one round of one token; warps take tasks token-major,
+// so a long row spreads over several warps (a 14 KB row with k = 8 over 14), and
+// every task's sources and weights are fetched while the previous task is summed.
+template <int SG, int CPL>
 __global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
   const int lane = threadIdx.x & 31;
   const int n16 = d.D / 8;
-  const int ntok = d.W * d.T;
+  const int nblk = (n16 + 32 * CPL - 1) / (32 * CPL);
+  const int ntask = d.W * d.T * nblk;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int src_n = INT_MIN;
   float w_n = 0.f;
-  if (tok < ntok && lane < d.k) {
+  if (task < ntask && lane < d.k) {
+    const int tok = task / nblk;
     src_n = __ldg(a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k + lane);
     w_n = __ldg(a.w + (size_t)tok * d.k + lane);
   }
-  for (; tok < ntok; tok += warps) {
+  for (; task < ntask; task += warps) {
     const int src_l = src_n;
     const float w_l = w_n;
-    const int nxt = tok + warps;
-    if (nxt < ntok && lane < d.k) {
-      src_n = __ldg(a.p.a[PA_SCALE_SRC] + (size_t)nxt * d.k + lane);
-      w_n = __ldg(a.w + (size_t)nxt * d.k + lane);
+    const int nxt = task + warps;
+    if (nxt < ntask && lane < d.k) {
+      const int tok = nxt / nblk;
+      src_n = __ldg(a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k + lane);
+      w_n = __ldg(a.w + (size_t)tok * d.k + lane);
     }
-    const int s = tok / d.T, t = tok % d.T;
-    uint4* out = reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D);
-    for (int c0 = 0; c0 < n16; c0 += 64) {
-      const int ca = c0 + lane, cb = c0 + 32 + lane;
-      float acc0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float acc1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j0 = 0; j0 < d.k; j0 += kScaleGroup) {
-        uint4 va[kScaleGroup], vb[kScaleGroup];
-        float wj[kScaleGroup];
-#pragma unroll
-        for (int q = 0; q < kScaleGroup; ++q) {
-          const int j = j0 + q;
-          const int sj = __shfl_sync(0xffffffffu, src_l, j & 31);
-          wj[q] = __shfl_sync(0xffffffffu, w_l, j & 31);
-          // Slots past k, and invalid routing slots (reported by the plan), add nothing.
-          const bool live = j < d.k && sj != INT_MIN;
-          if (!live) wj[q] = 0.f;
-          const uint4* row = reinterpret_cast<const uint4*>(
-              sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D);
-          va[q] = live && ca < n16 ? __ldg(row + ca) : make_uint4(0, 0, 0, 0);
-          vb[q] = live && cb < n16 ? __ldg(row + cb) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int q = 0; q < kScaleGroup; ++q) {
-          fma_bf16x8(acc0, wj[q], va[q]);
-          fma_bf16x8(acc1, wj[q], vb[q]);
-        }
-      }
-      if (ca < n16)
-        out[ca] = make_uint4(pack_bf16x2(acc0[0], acc0[1]), pack_bf16x2(acc0[2], acc0[3]),
-                             pack_bf16x2(acc0[4], acc0[5]), pack_bf16x2(acc0[6], acc0[7]));
-      if (cb < n16)
-        out[cb] = make_uint4(pack_bf16x2(acc1[0], acc1[1]), pack_bf16x2(acc1[2], acc1[3]),
-                             pack_bf16x2(acc1[4], acc1[5]), pack_bf16x2(acc1[6], acc1[7]));
-    }
-  }
-}
-
-// scale_kernel's sum of one token (s, t), for rows that a kernel still running
-// beside this one has written: the same operations in the same order (so the same
-// bits), but the rows are read from L2 (__ldcg), since the read-only and L1 paths
-// are not kept coherent with such writes. Lane j < k holds slot j's source and
-// weight.
-__device__ __forceinline__ void scale_token_l2(const ScaleArgs& a, int s, int t, int src_l,
-                                               float w_l, int lane) {
-  const Dims d = a.p.d;
-  const int n16 = d.D / 8;
-  uint4* out = reinterpret_cast<uint4*>(a.out[s] + (size_t)t * d.D);
-  for (int c0 = 0; c0 < n16; c0 += 64) {
-    const int ca = c0 + lane, cb = c0 + 32 + lane;
-    float acc0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float acc1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j0 = 0; j0 < d.k; j0 += kScaleGroup) {
-      uint4 va[kScaleGroup], vb[kScaleGroup];
-      float wj[kScaleGroup];
-#pragma unroll
-      for (int q = 0; q < kScaleGroup; ++q) {
-        const int j = j0 + q;
-        const int sj = __shfl_sync(0xffffffffu, src_l, j & 31);
-        wj[q] = __shfl_sync(0xffffffffu, w_l, j & 31);
-        // Slots past k, and invalid routing slots (reported by the plan), add nothing.
-        const bool live = j < d.k && sj != INT_MIN;
-        if (!live) wj[q] = 0.f;
-        const uint4* row = reinterpret_cast<const uint4*>(
-            sj >= 0 ? a.recv[s] + (size_t)sj * d.D : a.y[s] + (size_t)(-sj - 1) * d.D);
-        va[q] = live && ca < n16 ? __ldcg(row + ca) : make_uint4(0, 0, 0, 0);
-        vb[q] = live && cb < n16 ? __ldcg(row + cb) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int q = 0; q < kScaleGroup; ++q) {
-        fma_bf16x8(acc0, wj[q], va[q]);
-        fma_bf16x8(acc1, wj[q], vb[q]);
-      }
-    }
-    if (ca < n16)
-      out[ca] = make_uint4(pack_bf16x2(acc0[0], acc0[1]), pack_bf16x2(acc0[2], acc0[3]),
-                           pack_bf16x2(acc0[4], acc0[5]), pack_bf16x2(acc0[6], acc0[7]));
-    if (cb < n16)
-      out[cb] = make_uint4(pack_bf16x2(acc1[0], acc1[1]), pack_bf16x2(acc1[2], acc1[3]),
-                           pack_bf16x2(acc1[4], acc1[5]), pack_bf16x2(acc1[6], acc1[7]));
+    const int tok = task / nblk;
+    scale_round<SG, CPL, false>(a, d, tok / d.T, tok % d.T, src_l, w_l, lane,
+                                (task % nblk) * 32 * CPL);
   }
 }
 
@@ -160,87 +139,101 @@ __device__ __forceinline__ void scale_token_l2(const ScaleArgs& a, int s, int t,
 // Perseus summary, section 4.1, Algorithm 1: the receiver acts on the one signal of
 // each (sender, destination) group). Launched right behind the producer (or the
 // consumer) on its stream as a programmatic dependent launch, so its CTAs are placed
-// only once every CTA of that kernel is resident, and run beside it. A token's sum
-// starts once its rows are final: for each remote slot the signal of its (sender,
-// destination) group, for each local slot the ready flags of the owner's band that
-// holds the row. Warps claim tokens 32 at a time from two counters of the plan
-// (zeroed by the combine): first the tokens whose slots are all remote (their groups
-// signal as the remote tiles finish, while the producer works through the local
-// ones), then the rest. The arithmetic is scale_kernel's: the same bits.
-constexpr int kScaleClaim = 32;
+// only once every CTA of that kernel is resident, and run beside it. Two gates, each
+// watched by one thread per CTA with long sleeps between reads (so the waiting CTAs
+// take almost nothing from the producer): first every (sender, destination) group
+// that sends rows has signalled, which makes every receive row final; then every
+// output tile of the producer has been counted, which makes every local row final.
+// Past the first gate the warps sum the tokens whose slots are all remote (their
+// rows are in the receive buffers), while the producer still works through the local
+// tiles it schedules last; past the second, the rest. Warps claim scale_kernel's tasks
+// eight at a time from two counters of the plan (zeroed by the combine), and sum them
+// with the same rounds: the same bits.
+constexpr int kScaleClaim = 8;
+constexpr int kGatePollNs = 1000;  // sleep between two reads of a gate
 
-__global__ void __launch_bounds__(256, 4) scale_gated_kernel(const __grid_constant__ ScaleArgs a) {
+template <int SG, int CPL>
+__global__ void __launch_bounds__(256) scale_gated_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
   const int lane = threadIdx.x & 31;
-  const int ntok = d.W * d.T;
+  const int n16 = d.D / 8;
+  const int nblk = (n16 + 32 * CPL - 1) / (32 * CPL);
+  const int ntask = d.W * d.T * nblk;
   uint32_t* status = reinterpret_cast<uint32_t*>(a.p.a[PA_STATUS]);
-  const uint32_t* flags = reinterpret_cast<const uint32_t*>(a.p.a[PA_FLAGS]);
   const uint32_t* gsig = reinterpret_cast<const uint32_t*>(a.p.a[PA_GROUP_SIG]);
-  uint32_t* claim = reinterpret_cast<uint32_t*>(a.p.a[PA_QUEUE]) + 1;  // [1], [2]: the passes
-  // First receive row of each sender at each destination: receive rows are ordered by
-  // sender rank, and a sender's first expert starts its range.
-  __shared__ int s_start[MOE_MAX_RANKS][MOE_MAX_RANKS];  // [destination][sender]
-  for (int i = threadIdx.x; i < d.W * d.W; i += blockDim.x) {
-    const int s = i / d.W, o = i % d.W;
-    s_start[s][o] = o == s ? INT_MAX : __ldg(a.p.a[PA_RECV_OFF] + (size_t)o * d.L * d.W + s);
+  uint32_t* queue = reinterpret_cast<uint32_t*>(a.p.a[PA_QUEUE]);
+  uint32_t* claim = queue + 1;  // [1], [2]: the token counters of the two passes
+  const uint32_t* tiles_done = queue + 3;  // output tiles (tile, N-tile) the producer finished
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    span_begin(a.p.span, kSpanScaleStart);
+    s_ok = 1;
   }
-  if (threadIdx.x == 0) span_begin(a.p.span, kSpanScaleStart);
-  __syncthreads();
-
-  unsigned long long seen = 0;  // groups (sender * W + destination) seen signalled, warp-uniform
   bool ok = true;
   for (int pass = 0; pass < 2 && ok; ++pass) {
-    while (ok) {
-      int base = 0;
-      if (lane == 0) base = (int)atomicAdd(claim + pass, (uint32_t)kScaleClaim);
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (base >= ntok) break;
-      for (int tok = base; tok < min(base + kScaleClaim, ntok) && ok; ++tok) {
-        int src = INT_MIN;
-        float wt = 0.f;
-        if (lane < d.k) {
-          src = __ldg(a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k + lane);
-          wt = __ldg(a.w + (size_t)tok * d.k + lane);
+    if (threadIdx.x == 0 && s_ok) {
+      // Bounded wait for this pass's gate, one read per kGatePollNs.
+      const unsigned long long t0 = globaltimer();
+      const uint32_t need = (uint32_t)a.p.a[PA_TOTALS][0] * (uint32_t)d.nt2;
+      int g = 0;
+      while (true) {
+        bool open;
+        if (pass == 0) {
+          while (g < d.W * d.W && (__ldg(a.p.a[PA_GROUP_NCHUNK] + g) == 0 ||
+                                   ld_relaxed_u32(gsig + g) != 0u))
+            ++g;
+          open = g == d.W * d.W;
+        } else {
+          open = ld_relaxed_u32(tiles_done) >= need;
         }
-        const bool local = src < 0 && src != INT_MIN;
-        if (__any_sync(0xffffffffu, local) != (pass == 1)) continue;
-        const int s = tok / d.T;
-        int g = -1;
-        if (src >= 0) {  // the sender: the last rank whose first receive row is <= src
-          int o = 0;
-          for (int q = 0; q < d.W; ++q)
-            if (s_start[s][q] <= src) o = q;
-          g = o * d.W + s;
+        if (open) break;
+        if (ld_relaxed_u32(status) != 0u) {
+          s_ok = 0;
+          break;
         }
-        const uint32_t* f = local ? flags + ((size_t)s * d.NBM + (-src - 1) / d.tb) * d.nt2 : nullptr;
-        // Bounded wait until every slot's rows are final (relaxed reads, then one
-        // acquire fence per lane before the row loads).
-        const unsigned long long t0 = globaltimer();
-        while (true) {
-          bool ready = true;
-          if (g >= 0 && !((seen >> g) & 1ull)) ready = ld_relaxed_u32(gsig + g) != 0u;
-          if (f != nullptr)
-            for (int i = 0; i < d.nt2; ++i) ready &= ld_relaxed_u32(f + i) >= (uint32_t)d.parts;
-          if (__all_sync(0xffffffffu, ready)) break;
-          bool stop = false;
-          if (lane == 0)
-            stop = ld_relaxed_u32(status) != 0u ||
-                   ((long long)(globaltimer() - t0) > a.p.timeout_ns &&
-                    (report_error(status, MOE_DEV_TIMEOUT, 0x70000000u | (uint32_t)tok), true));
-          if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) {
-            ok = false;
-            break;
-          }
-          __nanosleep(256);
+        if ((long long)(globaltimer() - t0) > a.p.timeout_ns) {
+          report_error(status, MOE_DEV_TIMEOUT, 0x70000000u | (uint32_t)pass);
+          s_ok = 0;
+          break;
         }
-        if (!ok) break;
-        fence_acq_rel_gpu();
-        __syncwarp();
-        const unsigned long long mine = g >= 0 ? 1ull << g : 0ull;
-        seen |= (unsigned long long)__reduce_or_sync(0xffffffffu, (uint32_t)mine) |
-                ((unsigned long long)__reduce_or_sync(0xffffffffu, (uint32_t)(mine >> 32)) << 32);
-        scale_token_l2(a, s, tok % d.T, src, wt, lane);
+        __nanosleep(kGatePollNs);
       }
+      fence_acq_rel_gpu();  // the reads that opened the gate become acquires
+    }
+    __syncthreads();
+    ok = s_ok != 0;
+    if (!ok) break;
+    fence_acq_rel_gpu();
+    // Tasks as in scale_kernel (one round of one token), claimed kScaleClaim at a
+    // time; a task whose token belongs to the other pass is skipped. The next task's
+    // sources and weights are fetched while the current one is summed.
+    int task = 0, end = 0;
+    int src_n = INT_MIN;
+    float w_n = 0.f;
+    auto fetch = [&](int tk) {
+      if (lane < d.k) {
+        const int tok = tk / nblk;
+        src_n = __ldg(a.p.a[PA_SCALE_SRC] + (size_t)tok * d.k + lane);
+        w_n = __ldg(a.w + (size_t)tok * d.k + lane);
+      }
+    };
+    while (true) {
+      if (task == end) {
+        int base = 0;
+        if (lane == 0) base = (int)atomicAdd(claim + pass, (uint32_t)kScaleClaim);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (base >= ntask) break;
+        task = base;
+        end = min(base + kScaleClaim, ntask);
+        fetch(task);
+      }
+      const int src = src_n;
+      const float wt = w_n;
+      const int tok = task / nblk, c0 = (task % nblk) * 32 * CPL;
+      if (++task < end) fetch(task);
+      const bool local = src < 0 && src != INT_MIN;
+      if (__any_sync(0xffffffffu, local) != (pass == 1)) continue;
+      scale_round<SG, CPL, true>(a, d, tok / d.T, tok % d.T, src, wt, lane, c0);
     }
   }
   __syncthreads();
@@ -250,8 +243,59 @@ __global__ void __launch_bounds__(256, 4) scale_gated_kernel(const __grid_consta
 }  // namespace
 
 namespace {
-int g_scale_blocks_per_sm = 0;  // resident scale blocks per SM (set at preload)
+// Resident blocks per SM of each scale kernel variant (k >= 4, k < 4), set at preload.
+int g_scale_blocks_per_sm[2] = {0, 0};
+
+int scale_variant(int k) { return k >= 4 ? 0 : 1; }
+
+template <int SG, int CPL>
+cudaError_t preload_scale_variant(int v) {
+  cudaFuncAttributes fa;
+  cudaError_t e;
+  if ((e = cudaFuncGetAttributes(&fa, scale_kernel<SG, CPL>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, scale_gated_kernel<SG, CPL>)) != cudaSuccess) return e;
+  int n = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scale_kernel<SG, CPL>, 256, 0)) !=
+      cudaSuccess)
+    return e;
+  g_scale_blocks_per_sm[v] = n;
+  return cudaSuccess;
 }
+
+// Blocks of a scale launch over `units` warp tasks: as many as fit on the GPU at once
+// (every warp then walks several tasks), fewer when there is less work.
+int scale_blocks(int v, long long units, int num_sms) {
+  const int per_sm = g_scale_blocks_per_sm[v] > 0 ? g_scale_blocks_per_sm[v] : 2;
+  return (int)std::max(1LL, std::min((units + 7) / 8, (long long)num_sms * per_sm));
+}
+
+template <int SG, int CPL>
+cudaError_t launch_scale_variant(const ScaleArgs& a, int num_sms, cudaStream_t s) {
+  const int n16 = a.p.d.D / 8;
+  const long long tasks = (long long)a.p.d.W * a.p.d.T * ((n16 + 32 * CPL - 1) / (32 * CPL));
+  scale_kernel<SG, CPL><<<scale_blocks(scale_variant(a.p.d.k), tasks, num_sms), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int SG, int CPL>
+cudaError_t launch_scale_gated_variant(const ScaleArgs& a, int num_sms, cudaStream_t s) {
+  // As many CTAs as the plain scale; those that do not fit beside the running kernel
+  // start as its CTAs leave. Programmatic stream serialization: the launch may begin
+  // once every CTA of the previous kernel on the stream has allowed it.
+  cudaLaunchConfig_t cfg = {};
+  const int n16 = a.p.d.D / 8;
+  const long long tasks = (long long)a.p.d.W * a.p.d.T * ((n16 + 32 * CPL - 1) / (32 * CPL));
+  cfg.gridDim = dim3((unsigned)scale_blocks(scale_variant(a.p.d.k), tasks, num_sms));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, scale_gated_kernel<SG, CPL>, a);
+}
+}  // namespace
 
 template <int PER>
 cudaError_t launch_route_per(const DevPlan& p, const float* logits, const int32_t* forced,
@@ -271,12 +315,8 @@ cudaError_t preload_route_scale() {
       (e = cudaFuncGetAttributes(&fa, route_kernel<16>)) != cudaSuccess ||
       (e = cudaFuncGetAttributes(&fa, route_kernel<32>)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncGetAttributes(&fa, scale_kernel)) != cudaSuccess) return e;
-  if ((e = cudaFuncGetAttributes(&fa, scale_gated_kernel)) != cudaSuccess) return e;
-  int n = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scale_kernel, 256, 0)) != cudaSuccess)
-    return e;
-  g_scale_blocks_per_sm = n;
+  if ((e = preload_scale_variant<4, 2>(0)) != cudaSuccess) return e;
+  if ((e = preload_scale_variant<2, 4>(1)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
@@ -292,31 +332,17 @@ cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* f
 }
 
 cudaError_t launch_scale(const ScaleArgs& a, int num_sms, cudaStream_t s) {
-  // Eight warps per block, one token per warp at a time; as many blocks as fit on
-  // the GPU at once, so every warp walks several tokens (and prefetches the next).
-  const int tokens = a.p.d.W * a.p.d.T;
-  const int per_sm = g_scale_blocks_per_sm > 0 ? g_scale_blocks_per_sm : 4;
-  const int blocks = std::min((tokens + 7) / 8, num_sms * per_sm);
-  scale_kernel<<<blocks, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  switch (scale_variant(a.p.d.k)) {
+    case 0: return launch_scale_variant<4, 2>(a, num_sms, s);
+    default: return launch_scale_variant<2, 4>(a, num_sms, s);
+  }
 }
 
 cudaError_t launch_scale_gated(const ScaleArgs& a, int num_sms, cudaStream_t s) {
-  // As many CTAs as the plain scale; those that do not fit beside the running kernel
-  // start as its CTAs leave. Programmatic stream serialization: the launch may begin
-  // once every CTA of the previous kernel on the stream has allowed it.
-  const int tokens = a.p.d.W * a.p.d.T;
-  const int per_sm = g_scale_blocks_per_sm > 0 ? g_scale_blocks_per_sm : 4;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)std::max(1, std::min((tokens + 7) / 8, num_sms * per_sm)));
-  cfg.blockDim = dim3(256);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, scale_gated_kernel, a);
+  switch (scale_variant(a.p.d.k)) {
+    case 0: return launch_scale_gated_variant<4, 2>(a, num_sms, s);
+    default: return launch_scale_gated_variant<2, 4>(a, num_sms, s);
+  }
 }
 
 }  // namespace moe
