@@ -130,7 +130,8 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_XPREV] = W * (size_t)d.RM;
   // Copy chunks of one combine: at most one partial chunk per segment beyond the
   // remote rows (at most W * T * topk) cut into chunks of rpc rows.
-  n[PA_CHUNK_T] = 2 * (W * (size_t)d.T * d.k / d.rpc + W * NBM + 1);
+  n[PA_CHUNK_REC] = W * (size_t)d.T * d.k / d.rpc + W * NBM + 1;
+  n[PA_CHUNK_T] = 2 * n[PA_CHUNK_REC];
   size_t pos = 0;
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;

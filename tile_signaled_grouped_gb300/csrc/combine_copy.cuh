@@ -8,44 +8,37 @@
 namespace moe {
 
 constexpr int kMaxGroups = MOE_MAX_RANKS * MOE_MAX_RANKS;
-constexpr int kListCap = kMaxSegChunks;  // owned chunks listed per batch of records
 
 // Shared memory of one copying warp: SLOTS chunk slots live elsewhere.
-template <int SLOTS, int REC_PER_LANE>
+template <int SLOTS>
 struct CopySmem {
   uint64_t full[SLOTS];
-  int stored[kMaxGroups];                   // chunks of each group stored since the last release
-  int rec[32 * REC_PER_LANE][kSegRec];      // a batch of segment records
-  int list[kListCap];                       // owned chunks of the batch: (record << 20) | chunk index
+  int stored[kMaxGroups];  // chunks of each group stored since the last release
+  int rec[32][kSegRec];    // the segment record of each lane's chunk of the current round
+  int cidx[32];            // that chunk's index inside its segment
 };
-
-// Chunks i in [cb, cb + n) with i % G == c.
-__device__ __forceinline__ int owned_count(int cb, int n, int c, int G) {
-  const int i0 = cb + ((c - cb) % G + G) % G;
-  return i0 >= cb + n ? 0 : (cb + n - 1 - i0) / G + 1;
-}
 
 // Copies every chunk i (of all segments, in the producer's tile order) with
 // i % G == c: waits for its ready flags, moves it Y -> receive buffer through
 // SLOTS shared-memory slots of kChunkBytes (at most INFLIGHT loads outstanding),
 // and releases the stored chunks per group at each wait and at the end. Called by
 // all 32 lanes of one warp.
-template <int SLOTS, int INFLIGHT, int REC_PER_LANE>
+template <int SLOTS, int INFLIGHT>
 __device__ __forceinline__ void combine_copy(const DevPlan& p, const __nv_bfloat16* const* y,
                                              __nv_bfloat16* const* recv, uint8_t* slots,
-                                             CopySmem<SLOTS, REC_PER_LANE>& sm, int c, int G) {
+                                             CopySmem<SLOTS>& sm, int c, int G) {
   static_assert(INFLIGHT >= 1 && INFLIGHT <= SLOTS, "copy ring");
   constexpr int kChunkSlots = SLOTS;
   constexpr int kLoadsInFlight = INFLIGHT;
-  constexpr int kRecPerLane = REC_PER_LANE;
   const Dims d = p.d;
   uint32_t* status = reinterpret_cast<uint32_t*>(p.a[PA_STATUS]);
   const uint32_t* flags = reinterpret_cast<const uint32_t*>(p.a[PA_FLAGS]);
   uint32_t* group_done = reinterpret_cast<uint32_t*>(p.a[PA_GROUP_DONE]);
   uint32_t* group_sig = reinterpret_cast<uint32_t*>(p.a[PA_GROUP_SIG]);
   const int32_t* recs = p.a[PA_SEG_REC];
+  const int32_t* chunk_rec = p.a[PA_CHUNK_REC];
   const int32_t* gchunks = p.a[PA_GROUP_NCHUNK];
-  const int nseg = p.a[PA_TOTALS][1];
+  const int nch = p.a[PA_TOTALS][4];
   const int lane = threadIdx.x & 31;
   const size_t row_bytes = (size_t)d.D * 2;
 
@@ -124,11 +117,9 @@ __device__ __forceinline__ void combine_copy(const DevPlan& p, const __nv_bfloat
     __syncwarp();
   };
 
-  // Rows and flags of listed chunk `e` (a packed list entry).
-  auto chunk_of = [&](int e, int& q, int& r0, int& r1) {
-    q = e >> 20;
-    const int k = e & 0xFFFFF;
-    r0 = k * d.rpc;
+  // Rows [r0, r1) of the segment that round entry q (a lane's chunk) copies.
+  auto chunk_rows = [&](int q, int& r0, int& r1) {
+    r0 = sm.cidx[q] * d.rpc;
     r1 = min(sm.rec[q][4], r0 + d.rpc);
   };
   // Relaxed reads of the ready flags of one chunk (a subset of them per lane), all
@@ -146,156 +137,97 @@ __device__ __forceinline__ void combine_copy(const DevPlan& p, const __nv_bfloat
     return ready;
   };
 
-  // Records are taken in batches of up to 32 * REC_PER_LANE (loads
-  // independent). Each batch lists this CTA's chunks of as many of its records as
-  // fit in kListCap entries, in order; the flags of 64 listed chunks are checked
-  // per round trip (2 per lane).
-  int base = 0;
-  while (base < nseg && ok) {
-    int cnt[kRecPerLane];
-    int lsum = 0;
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < kRecPerLane; ++u) {
-      const int ri = lane * kRecPerLane + u;  // record of the batch, in order
-      const int idx = base + ri;
-      cnt[u] = 0;
-      if (idx < nseg) {
-        const int4* r = reinterpret_cast<const int4*>(recs + (size_t)idx * kSegRec);
-        const int4 lo = r[0], hi = r[1];
-        sm.rec[ri][0] = lo.x; sm.rec[ri][1] = lo.y; sm.rec[ri][2] = lo.z; sm.rec[ri][3] = lo.w;
-        sm.rec[ri][4] = hi.x; sm.rec[ri][5] = hi.y; sm.rec[ri][6] = hi.z; sm.rec[ri][7] = hi.w;
-        cnt[u] = owned_count(hi.z, hi.w, c, G);
-      }
-      lsum += cnt[u];
+  // This warp's chunks are c, c + G, c + 2G, ... of the global sequence, and the plan
+  // maps every chunk to its segment record. A round takes the next 32 of them, one
+  // per lane: each lane reads its chunk's record and the chunk's ready flags (all
+  // lanes' reads in flight together); then lane 0 moves the round's chunks in order,
+  // waiting (bounded, all lanes) where a chunk is not produced yet.
+  for (long long m0 = 0; ok; m0 += 32) {
+    const long long i = (long long)c + (m0 + lane) * G;
+    const bool have = i < nch;
+    const int m = __popc(__ballot_sync(0xffffffffu, have));  // lanes 0 .. m-1
+    if (m == 0) break;
+    __syncwarp();  // lane 0 no longer reads the previous round's records
+    bool rdy = true;
+    if (have) {
+      const int q = __ldg(chunk_rec + i);
+      const int4* r = reinterpret_cast<const int4*>(recs + (size_t)q * kSegRec);
+      const int4 lo = __ldg(r), hi = __ldg(r + 1);
+      sm.rec[lane][0] = lo.x; sm.rec[lane][1] = lo.y; sm.rec[lane][2] = lo.z; sm.rec[lane][3] = lo.w;
+      sm.rec[lane][4] = hi.x; sm.rec[lane][5] = hi.y; sm.rec[lane][6] = hi.z; sm.rec[lane][7] = hi.w;
+      sm.cidx[lane] = (int)(i - hi.z);
+      int r0, r1;
+      chunk_rows(lane, r0, r1);
+      rdy = flags_ready(lane, r0, r1, 0, 1);
     }
-    int incl = lsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    // Records that fit: a prefix of the batch (the first record always fits,
-    // because a segment has at most kListCap chunks).
-    int pos = incl - lsum, fit = 0;
-#pragma unroll
-    for (int u = 0; u < kRecPerLane; ++u) {
-      const int idx = base + lane * kRecPerLane + u;
-      if (idx < nseg && pos + cnt[u] <= kListCap) {
-        const int ri = lane * kRecPerLane + u;
-        int k = ((c - sm.rec[ri][6]) % G + G) % G;
-        for (int j = 0; j < cnt[u]; ++j, k += G) sm.list[pos + j] = (ri << 20) | k;
-        pos += cnt[u];
-        ++fit;
-      } else {
-        pos = kListCap + 1;  // later records of the batch wait for the next batch
-      }
-    }
-    int take = fit;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) take += __shfl_xor_sync(0xffffffffu, take, o);
-    take = max(1, take);
-    int nlist = 0;
-    {  // entries written by the fitting records
-      const int last = take - 1;  // last fitting record of the batch
-      const int ll = last / kRecPerLane;
-      int e = incl - lsum;
-      for (int u = 0; u <= last - ll * kRecPerLane; ++u) e += cnt[u];
-      nlist = __shfl_sync(0xffffffffu, e, ll);
-    }
-    __syncwarp();
-
-    for (int s0 = 0; s0 < nlist && ok; s0 += 64) {
-      const int m = min(64, nlist - s0);
-      bool r0ok = true, r1ok = true;
-      if (lane < m) {
-        int q, a0, a1;
-        chunk_of(sm.list[s0 + lane], q, a0, a1);
-        r0ok = flags_ready(q, a0, a1, 0, 1);
-      }
-      if (lane + 32 < m) {
-        int q, a0, a1;
-        chunk_of(sm.list[s0 + 32 + lane], q, a0, a1);
-        r1ok = flags_ready(q, a0, a1, 0, 1);
-      }
-      unsigned long long ready = (unsigned long long)__ballot_sync(0xffffffffu, r0ok) |
-                                 ((unsigned long long)__ballot_sync(0xffffffffu, r1ok) << 32);
-      fence_acq_rel_gpu();  // each lane: its flag reads become acquires
-      __syncwarp();         // orders lane 0's copies after every lane's acquire
-      // The flags were acquired (generic proxy); the bulk loads read Y (async proxy).
-      if (lane == 0) fence_proxy_async_global();
-      for (int j = 0; j < m && ok; ++j) {
-        int q, r0, r1;
-        chunk_of(sm.list[s0 + j], q, r0, r1);
-        if (!(ready >> j & 1ull)) {
-          // Not produced yet: store everything loaded, release the stored chunks,
-          // then wait (bounded, all lanes).
-          if (lane == 0)
-            while (stored < n) store_one();
-          release_stored();
-          const unsigned long long t0 = globaltimer();
-          bool done = false, stop = false;
-          while (!done && !stop) {
-            done = __all_sync(0xffffffffu, flags_ready(q, r0, r1, lane, 32));
-            if (!done) {
-              __nanosleep(64);
-              if (lane == 0) {
-                if (ld_relaxed_u32(status) != 0) {
-                  stop = true;
-                } else if ((long long)(globaltimer() - t0) > p.timeout_ns) {
-                  const int bl = sm.rec[q][2] + r0 / d.tb;
-                  report_error(status, MOE_DEV_TIMEOUT,
-                               0x50000000u | (uint32_t)((size_t)sm.rec[q][0] * d.NBM + bl));
-                  stop = true;
-                }
+    unsigned ready = __ballot_sync(0xffffffffu, rdy);
+    fence_acq_rel_gpu();  // each lane: its flag reads become acquires
+    __syncwarp();         // orders lane 0's copies after every lane's acquire (and records)
+    // The flags were acquired (generic proxy); the bulk loads read Y (async proxy).
+    if (lane == 0) fence_proxy_async_global();
+    for (int j = 0; j < m && ok; ++j) {
+      int r0, r1;
+      chunk_rows(j, r0, r1);
+      if (!(ready >> j & 1u)) {
+        // Not produced yet: store everything loaded, release the stored chunks,
+        // then wait (bounded, all lanes).
+        if (lane == 0)
+          while (stored < n) store_one();
+        release_stored();
+        const unsigned long long t0 = globaltimer();
+        bool done = false, stop = false;
+        while (!done && !stop) {
+          done = __all_sync(0xffffffffu, flags_ready(j, r0, r1, lane, 32));
+          if (!done) {
+            __nanosleep(64);
+            if (lane == 0) {
+              if (ld_relaxed_u32(status) != 0) {
+                stop = true;
+              } else if ((long long)(globaltimer() - t0) > p.timeout_ns) {
+                const int bl = sm.rec[j][2] + r0 / d.tb;
+                report_error(status, MOE_DEV_TIMEOUT,
+                             0x50000000u | (uint32_t)((size_t)sm.rec[j][0] * d.NBM + bl));
+                stop = true;
               }
-              stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
             }
+            stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
           }
-          if (stop) {
-            ok = false;
-            break;
-          }
-          // Chunks after this one may have become ready meanwhile.
-          bool a0ok = true, a1ok = true;
-          if (lane > j && lane < m) {
-            int q2, b0, b1;
-            chunk_of(sm.list[s0 + lane], q2, b0, b1);
-            a0ok = flags_ready(q2, b0, b1, 0, 1);
-          }
-          if (lane + 32 > j && lane + 32 < m) {
-            int q2, b0, b1;
-            chunk_of(sm.list[s0 + 32 + lane], q2, b0, b1);
-            a1ok = flags_ready(q2, b0, b1, 0, 1);
-          }
-          ready = (unsigned long long)__ballot_sync(0xffffffffu, a0ok) |
-                  ((unsigned long long)__ballot_sync(0xffffffffu, a1ok) << 32);
-          ready |= j == 63 ? ~0ull : ((1ull << (j + 1)) - 1ull);
-          fence_acq_rel_gpu();
-          __syncwarp();
-          if (lane == 0) fence_proxy_async_global();
         }
-        if (lane == 0) {
-          store_landed();
-          while (n - stored >= kLoadsInFlight) store_one();
-          if (n >= kChunkSlots) bulk_wait_read<kChunkSlots - kLoadsInFlight>();
-          const int o = sm.rec[q][0], dst = sm.rec[q][1], b0 = sm.rec[q][2];
-          const int slot = n % kChunkSlots;
-          const uint32_t bytes = (uint32_t)((size_t)(r1 - r0) * row_bytes);
-          const uint8_t* src =
-              reinterpret_cast<const uint8_t*>(y[o]) + ((size_t)b0 * d.tb + r0) * row_bytes;
-          pend[slot].dst =
-              reinterpret_cast<uint8_t*>(recv[dst]) + ((size_t)sm.rec[q][5] + r0) * row_bytes;
-          pend[slot].bytes = bytes;
-          pend[slot].group = o * d.W + dst;
-          mbar_arrive_expect_tx(&sm.full[slot], bytes);
-          bulk_load(slots + (size_t)slot * kChunkBytes, src, bytes, &sm.full[slot]);
-          ++n;
+        if (stop) {
+          ok = false;
+          break;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        // Chunks after this one may have become ready meanwhile.
+        bool again = true;
+        if (lane > j && lane < m) {
+          int b0, b1;
+          chunk_rows(lane, b0, b1);
+          again = flags_ready(lane, b0, b1, 0, 1);
+        }
+        ready = __ballot_sync(0xffffffffu, again) | (j == 31 ? 0xffffffffu : (2u << j) - 1u);
+        fence_acq_rel_gpu();
+        __syncwarp();
+        if (lane == 0) fence_proxy_async_global();
       }
+      if (lane == 0) {
+        store_landed();
+        while (n - stored >= kLoadsInFlight) store_one();
+        if (n >= kChunkSlots) bulk_wait_read<kChunkSlots - kLoadsInFlight>();
+        const int o = sm.rec[j][0], dst = sm.rec[j][1], b0 = sm.rec[j][2];
+        const int slot = n % kChunkSlots;
+        const uint32_t bytes = (uint32_t)((size_t)(r1 - r0) * row_bytes);
+        const uint8_t* src =
+            reinterpret_cast<const uint8_t*>(y[o]) + ((size_t)b0 * d.tb + r0) * row_bytes;
+        pend[slot].dst =
+            reinterpret_cast<uint8_t*>(recv[dst]) + ((size_t)sm.rec[j][5] + r0) * row_bytes;
+        pend[slot].bytes = bytes;
+        pend[slot].group = o * d.W + dst;
+        mbar_arrive_expect_tx(&sm.full[slot], bytes);
+        bulk_load(slots + (size_t)slot * kChunkBytes, src, bytes, &sm.full[slot]);
+        ++n;
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
-    base += take;
   }
   // Drain: store what was loaded (even after an error, so no copy outlives the
   // CTA's shared memory), release the stored chunks, wait for every store.

@@ -13,8 +13,9 @@
 // pair producer): each segment is cut into chunks of rpc rows (up to 20 KB); the
 // chunks of all segments, in the producer's tile order, are dealt round-robin to
 // the consumer CTAs, so every CTA follows production and the last segment is
-// copied by all of them. A CTA is one warp: the lanes poll the flags of a chunk's
-// bands together, and lane 0 moves the chunk with TMA bulk copies through a
+// copied by all of them. A CTA is one warp: in rounds of 32 of its chunks, each lane
+// reads one chunk's segment record (through the plan's chunk-to-record map) and
+// polls its flags, and lane 0 moves the chunks with TMA bulk copies through a
 // six-slot shared-memory ring (global -> shared completes on an mbarrier,
 // shared -> global as a bulk group). A group is (sender o, destination s). At
 // each wait for the producer, and at its end, a CTA waits for its stores, issues
@@ -26,7 +27,7 @@
 namespace moe {
 namespace {
 
-using ConsumerSmem = CopySmem<kChunkSlots, 8>;
+using ConsumerSmem = CopySmem<kChunkSlots>;
 static_assert(sizeof(ConsumerSmem) <= kConsumerSmemTail, "consumer shared memory layout");
 
 __global__ void __launch_bounds__(kConsumerThreads, 1)
@@ -35,8 +36,8 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   allow_dependent_launch();  // a scale launched behind this kernel may start beside it
   ConsumerSmem& sm =
       *reinterpret_cast<ConsumerSmem*>(smem_raw + (size_t)kChunkSlots * kChunkBytes);
-  combine_copy<kChunkSlots, kLoadsInFlight, 8>(a.p, a.y, a.recv, smem_raw, sm, blockIdx.x,
-                                               gridDim.x);
+  combine_copy<kChunkSlots, kLoadsInFlight>(a.p, a.y, a.recv, smem_raw, sm, blockIdx.x,
+                                            gridDim.x);
 }
 
 }  // namespace

@@ -87,7 +87,7 @@ struct PSmem {
 
 // The fused variant also runs the combine copy in warp kCopyWarp: one chunk slot
 // and the copy state, paid for with one pipeline stage.
-using PairCopySmem = CopySmem<1, 2>;
+using PairCopySmem = CopySmem<1>;
 template <bool FUSED>
 struct PairCfg {
   static constexpr int kStages = FUSED ? kPMaxStages - 1 : kPMaxStages;
@@ -303,7 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
     // Every CTA of the grid copies its share of the finished segments (chunk i
     // when i % grid == CTA index), polling the ready flags, exactly as the
     // standalone consumer does on its own SMs.
-    combine_copy<1, 1, 2>(a.p, a.y, a.recv, copy_slot, csm, blockIdx.x, gridDim.x);
+    combine_copy<1, 1>(a.p, a.y, a.recv, copy_slot, csm, blockIdx.x, gridDim.x);
   } else if (warp == kSchedWarp && lane == 0) {
     // ------------------------------------------------------------ scheduler
     // Takes every ticket (rank 0 from the counter, handing it to rank 1), decodes

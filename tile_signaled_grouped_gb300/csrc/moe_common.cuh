@@ -77,6 +77,7 @@ enum PlanArray {
   PA_SPANS,  // [kSpanRing][kSpanWords] u64: device-clock records of each combine while timing
   PA_XPREV,  // [W][RM] what each X row held after the last gather: token, -1 zero, else unknown
   PA_CHUNK_T,  // [chunks] u64: device clock when each copy chunk had landed (timing on)
+  PA_CHUNK_REC,  // [chunks] segment record (consumer order) of every copy chunk
   PA_COUNT
 };
 

@@ -548,7 +548,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
   __syncthreads();
 
   // 4. One record per segment in consumer order: source band, destination, rows,
-  // and its range of copy chunks (rpc rows each) in the global chunk sequence.
+  // and its range of copy chunks (rpc rows each) in the global chunk sequence; and
+  // the record of every chunk.
   int chunk_carry = 0;
   for (int base = 0; base < nsegs; base += nt) {
     const int idx = base + tid;
@@ -579,6 +580,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
       int32_t* out = p.a[PA_SEG_REC] + (size_t)idx * kSegRec;
 #pragma unroll
       for (int q = 0; q < kSegRec; ++q) out[q] = rec[q];
+      for (int k = 0; k < nch; ++k) p.a[PA_CHUNK_REC][cb + k] = idx;
     }
     chunk_carry += tot;
   }
