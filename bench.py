@@ -170,6 +170,15 @@ def gpu_arm(args, rank, world, local_rank):
         wl = get_workload(args.workload, T=args.tokens_per_rank)
     W, T, D, F, k = wl.W, wl.T, wl.d_model, wl.d_ff, wl.topk
     inp = make_inputs(wl, device="cuda")
+    # --route gate: every step routes from the token rows with the gate kernel (router
+    # scores, softmax and top-k in one launch; a prescribed routing keeps its ids), and
+    # the plan starts from the counts the gate's routing tail wrote.
+    wr = None
+    if args.route == "gate":
+        from tile_signaled_grouped_gb300.workloads import router_weights
+        if wl.E > 256:
+            raise SystemExit(f"the gate kernel takes E <= 256 experts ({wl.name} has {wl.E})")
+        wr = router_weights(wl, device="cuda")
     torch.cuda.synchronize()  # inputs are drawn on the default stream; the steps run on sp/sc
     # Batches in flight: instance i % n (own plan and workspaces, own streams) runs
     # step i, so one batch's routing, plan and gather overlap the previous batch's
@@ -187,8 +196,9 @@ def gpu_arm(args, rank, world, local_rank):
     def step():
         j = step_i[0] % n_fly
         step_i[0] += 1
-        layers[j].forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
-                          producer=sps[j], consumer=scs[j])
+        layers[j].forward(inp.x, inp.w_gate, inp.w_up, inp.w_down,
+                          None if wr is not None else inp.logits, inp.forced_ids,
+                          producer=sps[j], consumer=scs[j], w_router=wr)
 
     for _ in range(max(args.warmup, n_fly)):
         step()
@@ -247,7 +257,7 @@ def gpu_arm(args, rank, world, local_rank):
 
     # ---- e2e through the C ABI with host buffers, right after the timed region (the
     # same power state: the GPU sits at its power cap within a fraction of a second) ---
-    e2e = e2e_arm(layers, inp, wl, sp, sc, args)
+    e2e = e2e_arm(layers, inp, wl, sp, sc, args, wr)
 
     # ---- stage measurements (outside the timed region) --------------------------------
     # They time kernels one at a time against the burst peaks, so they start from a
@@ -296,6 +306,8 @@ def gpu_arm(args, rank, world, local_rank):
                    else "one CTA per tile (M=128)",
                    "scale": ("overlapped with the producer (moe_scale_gated)"
                              if args.scale == "gated" else "after the combine (moe_scale)"),
+                   "routing": ("gate kernel from the token rows (seeded router)" if wr is not None
+                               else "from the drawn gate logits"),
                    "producer_ctas": launch[0], "consumer_ctas_launched": launch[1],
                    "num_sms": launch[2], "pair_clusters_resident": launch[3],
                    "parallelism": f"{W} logical EP ranks on 1 GPU; replicas x{world}",
@@ -313,8 +325,10 @@ def gpu_arm(args, rank, world, local_rank):
                      "per_step_tflops": per_step, "per_step_frac": per_step / peak,
                      "per_step_source": "executed FLOPs of one step / ms_per_step"},
         "e2e": e2e,
-        # route 1 + plan 5 + gather 1 + producer 1 + scale 1, + consumer kernel 1 unless fused
-        "gpu_launches": (9 + (0 if args.consumer_ctas < 0 else 1)) * args.steps,
+        # route 1 + plan 5 + gather 1 + producer 1 + scale 1, + consumer kernel 1 unless
+        # fused; routed by the gate: gate 1 + plan 3 (the gate wrote the counts)
+        "gpu_launches": ((9 if wr is None else 7) + (0 if args.consumer_ctas < 0 else 1))
+        * args.steps,
         "clocks": clk.summary(),
         "stages": stages,
         "work": {"rows_executed": rows_exec, "rows_valid": valid_rows,
@@ -352,25 +366,31 @@ def measure_gate(lay, x, wl, stream, iters, warmup, hbm):
     for _ in range(warmup):
         lay.gate(x, wr, stream=stream)
     torch.cuda.synchronize()
-    g = []
+    g, gs = [], []
     for _ in range(iters):
         with torch.cuda.stream(stream):
             flush.zero_()
         lay.set_timing(True)
         lay.gate(x, wr, stream=stream)
-        g.append(lay.timings()[0])
+        t = lay.timings()
+        g.append(t[0])
+        gs.append(t[9])
         lay.set_timing(False)
     code, detail = lay.status()
     if code != 0:
         raise RuntimeError(f"device status {code} detail {detail} in the gate kernel")
     ms = statistics.median(g)
+    span = statistics.median(gs)
     nbytes = 2.0 * D * W * T + 2.0 * D * wl.E + 8.0 * W * T * k
     flops = 2.0 * W * T * D * wl.E
     return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
             "tflops": flops / (ms * 1e-3) / 1e12,
             "timing": "CUDA events around the launch (launch latency included), "
-                      "L2 flushed before each, median of %d" % iters}
+                      "L2 flushed before each, median of %d" % iters,
+            "span_ms": span, "span_gbs": nbytes / (span * 1e-3) / 1e9,
+            "span_frac_hbm": nbytes / (span * 1e-3) / 1e9 / hbm,
+            "span_timing": "device clock, first CTA start to last CTA end, median"}
 
 
 def gate_arm(args):
@@ -414,6 +434,8 @@ def gate_arm(args):
                    "d_model": wl.d_model, "l2": "flushed before each launch"},
         "roofline": {"kernel": "gate_kernel", "bound": "hbm", "achieved": g["gbs"],
                      "peak": hbm, "unit": "GB/s", "frac": g["frac_hbm"], "traffic": None,
+                     "span_ms": g["span_ms"], "span_achieved": g["span_gbs"],
+                     "span_frac": g["span_frac_hbm"], "span_timing": g["span_timing"],
                      "peak_source": f"{src} HBM copy", "bytes_per_launch": g["bytes"],
                      "launch_ms": g["ms"], "launch_ms_source": g["timing"]},
         "tflops": g["tflops"],
@@ -568,7 +590,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     }
 
 
-def e2e_arm(layers, inp, wl, sp, sc, args):
+def e2e_arm(layers, inp, wl, sp, sc, args, wr=None):
     """Same metric through the public API with pinned host buffers: every step copies its
     inputs in and its output out inside the timed region. The runtime's HostPipeline
     overlaps step i+1's input copy and step i-1's output copy with step i's compute."""
@@ -578,16 +600,17 @@ def e2e_arm(layers, inp, wl, sp, sc, args):
 
     W, T, D = wl.W, wl.T, wl.d_model
     hx = [t.cpu().pin_memory() for t in inp.x]
-    hl = inp.logits.cpu().pin_memory()
+    hl = None if wr is not None else inp.logits.cpu().pin_memory()  # the gate needs no logits
     hf = None if inp.forced_ids is None else inp.forced_ids.cpu().pin_memory()
     hout = [torch.empty(T, D, dtype=torch.bfloat16).pin_memory() for _ in range(W)]
-    h2d = sum(t.numel() * t.element_size() for t in hx) + hl.numel() * 4 + \
+    h2d = sum(t.numel() * t.element_size() for t in hx) + (0 if hl is None else hl.numel() * 4) + \
         (0 if hf is None else hf.numel() * 4)
     d2h = sum(t.numel() * t.element_size() for t in hout)
     pipe = HostPipeline(layers, sp, sc, forced=hf is not None)
 
     def step(start_after=None):
-        pipe.step(hx, hl, hf, hout, inp.w_gate, inp.w_up, inp.w_down, start_after=start_after)
+        pipe.step(hx, hl, hf, hout, inp.w_gate, inp.w_up, inp.w_down, start_after=start_after,
+                  w_router=wr)
 
     for _ in range(3):
         step()
@@ -696,6 +719,10 @@ def main():
                     help="after: moe_scale once the combine is done; gated: moe_scale_gated, "
                          "launched behind the producer, waits on the device for each token's "
                          "group signals and ready flags")
+    ap.add_argument("--route", default="logits", choices=["logits", "gate"],
+                    help="logits: route from the drawn gate logits; gate: the gate kernel scores "
+                         "the token rows with a seeded router (softmax and top-k in the same "
+                         "launch) and writes the plan's counts")
     ap.add_argument("--producer-pairs", type=int, default=1, choices=[0, 1],
                     help="1: the CTA-pair producer (clusters of two, tcgen05 cta_group::2)")
     ap.add_argument("--gate-only", action="store_true",

@@ -135,8 +135,13 @@ int moe_route(moe_plan *plan, const float *logits, const int32_t *forced_ids,
  *              cluster share a 128-token tile, each summing a range of D; their
  *              partial sums are added in a fixed order, so a given split gives
  *              the same bits on every call).
+ * Each tile holds as many tokens (a multiple of 8, at most 128) as fill one wave of
+ * CTAs. The routing tail also writes the plan's token bitmaps, and the CTA that
+ * finishes last the group sizes and word prefixes (ids out of range or repeated set
+ * MOE_DEV_ROUTING), for a following moe_plan_build(plan, NULL, ...).
  * E <= 256; larger E, or a split the GPU cannot hold, gives MOE_ERR_UNSUPPORTED.
- * The caller owns every buffer. Timed in slot [0] of moe_timings. */
+ * The caller owns every buffer. Timed in slot [0] of moe_timings, its device-clock
+ * span in slot [9]. */
 int moe_gate(moe_plan *plan, const void *const *x, const void *w_router,
              const int32_t *forced_ids, int32_t *topk_ids, float *topk_w, float *logits,
              int splits, moe_stream_t stream);
@@ -144,7 +149,10 @@ int moe_gate(moe_plan *plan, const void *const *x, const void *w_router,
 /* Expert problem construction and combine plan (TileMoE notes section 4.2, 4.4
  * Algorithm 1, 4.5, 5.2) for all ranks, then the layout gather that fills each
  * owner's expert input X with its tokens' rows (zero rows for padding).
- *  topk_ids: [W][T][topk] int32, ids distinct within a token.
+ *  topk_ids: [W][T][topk] int32, ids distinct within a token; or NULL: the routing of
+ *            the last moe_gate on this plan (no moe_route or moe_plan_build since),
+ *            whose routing tail already wrote the token bitmaps and group counts, so
+ *            two plan kernels are skipped; MOE_ERR_ARG if there is none.
  *  x:        W pointers, rank s's tokens [T][D] bf16.
  * Ids out of range or repeated set MOE_DEV_ROUTING; the offending assignments are
  * skipped. No device-to-host transfer: every size is read on the device. */
@@ -310,7 +318,8 @@ int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count)
  * means over the last 64 combines: [6] the producer's execution span (its first CTA's
  * start to its last CTA's end; unlike [2] it excludes time spent queued behind other
  * kernels, for example those of another batch in flight), [7] the span of
- * moe_scale_gated, [8] the part of [7] before the producer's end. A slot with no
+ * moe_scale_gated, [8] the part of [7] before the producer's end, [9] the span of
+ * moe_gate. A slot with no
  * measurement is -1. Instrumentation only: moe_set_timing(plan, 1) records the events
  * and the device-clock records, 2 only the device-clock records (no CUDA event enters
  * the streams, so kernels keep overlapping as without timing), 0 nothing; enabling

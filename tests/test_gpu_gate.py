@@ -256,3 +256,54 @@ def test_captured_step_from_the_router_replays_bit_exactly():
     assert all(torch.equal(a, b) for a, b in zip(eager, layer.out))
     del graph
     layer.close()
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+@pytest.mark.parametrize("wl", [GATE_SHAPES[0], GATE_SHAPES[2], GATE_SHAPES[4],
+                                get_workload("qwen3_235b_like", routing="gate"),
+                                get_workload("a100_like")], ids=lambda w: w.name)
+def test_gate_writes_the_plan_counts(wl, splits):
+    """The gate's routing tail sets the plan's token bitmaps and its last CTA the group
+    sizes and word prefixes: the plan built from them (moe_plan_build with NULL ids, two
+    plan kernels fewer) equals, array for array, the plan the plan kernels build from
+    the same ids."""
+    inp = make_inputs(wl, device="cuda", with_weights=False)
+    wr = router_weights(wl, device="cuda")
+    layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb)
+    torch.cuda.synchronize()
+    layer.gate(inp.x, wr, inp.forced_ids, splits=splits)
+    layer.plan_build(inp.x, from_gate=True)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    names = [n for n in capi.ENUMS if n.startswith("MOE_PLAN_")
+             and n not in ("MOE_PLAN_NFIELDS", "MOE_PLAN_FLAGS", "MOE_PLAN_GROUP_SIG")]
+    from_gate = {n: layer.field(capi.ENUMS[n]).clone() for n in names}
+    layer.plan_build(inp.x, ids=layer.ids)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    for n in names:
+        assert torch.equal(from_gate[n], layer.field(capi.ENUMS[n])), n
+    with pytest.raises(capi.MoeError, match="ARG"):  # no gate since the last build
+        layer.plan_build(inp.x, from_gate=True)
+    layer.close()
+
+
+def test_gate_reports_bad_prescribed_ids():
+    """Prescribed ids out of range or repeated: the gate's routing tail reports the
+    first token (MOE_DEV_ROUTING), like the plan build does."""
+    wl = GATE_SHAPES[0]
+    inp = make_inputs(wl, device="cuda", with_weights=False)
+    wr = router_weights(wl, device="cuda")
+    layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb)
+    forced = torch.stack([torch.arange(wl.T) % wl.E, (torch.arange(wl.T) + 1) % wl.E],
+                         dim=-1).to(torch.int32).expand(wl.W, wl.T, 2).contiguous().cuda()
+    forced[2, 17, 1] = forced[2, 17, 0]  # repeated within the token
+    torch.cuda.synchronize()
+    layer.gate(inp.x, wr, forced)
+    torch.cuda.synchronize()
+    assert layer.status() == (capi.MOE_DEV_ROUTING, 2 * wl.T + 17)
+    layer.clear_status()
+    layer.gate(inp.x, wr)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    layer.close()

@@ -46,6 +46,8 @@ struct moe_plan {
   bool timing;        // CUDA events around each kernel
   bool spans;         // device-clock records (span ring, chunk landing stamps)
   bool gated_armed;   // a combine was enqueued since the last moe_scale_gated
+  bool gate_counted;  // the last routing call was moe_gate: its bitmaps and counts are in the plan
+  const int32_t* gate_ids;  // the ids that moe_gate wrote
 };
 
 namespace moe {
@@ -107,6 +109,7 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_FLAGS] = W * NBM * d.nt2;
   n[PA_GROUP_DONE] = W * W;
   n[PA_GROUP_SIG] = W * W;
+  n[PA_GATE_DONE] = 4;
   n[PA_BITMAP] = E * W * d.TW;
   n[PA_WPRE] = E * W * d.TW;
   n[PA_CNT] = n[PA_GROUP_START] = n[PA_RECV_OFF] = E * W;
@@ -359,6 +362,7 @@ int moe_route(moe_plan* p, const float* logits, const int32_t* forced, int32_t* 
   tstart(p, kTRoute, s);
   CUDA_TRY(launch_route(dp, logits, forced, ids, w, s));
   tstop(p, kTRoute, s);
+  p->gate_counted = false;
   return MOE_OK;
 }
 
@@ -373,9 +377,6 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
   if (p->gate_npad == 0 || (splits != 0 && p->gate_clusters[lg] == 0)) return MOE_ERR_UNSUPPORTED;
   GateArgs ga{};
   ga.npad = p->gate_npad;
-  for (int r = 0; r < d.W; ++r)
-    if (!aligned16(x[r]) || !make_map(p, &ga.tm_x[r], x[r], d.T, d.D, kTileM)) return MOE_ERR_ARG;
-  if (!make_map(p, &ga.tm_r, w_router, d.E, d.D, (uint32_t)ga.npad)) return MOE_ERR_ARG;
   ga.forced = forced;
   ga.ids = ids;
   ga.w = w;
@@ -391,22 +392,55 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
       if (tiles <= p->gate_clusters[i] && nk >= (4 << i)) splits = 1 << i;
   }
   ga.splits = splits;
+  // Tokens per tile: as few (a multiple of 8, at most 128) as fill one wave of
+  // clusters, so that every SM streams its share of the token rows.
+  {
+    const int lg = splits == 8 ? 3 : splits == 4 ? 2 : splits == 2 ? 1 : 0;
+    const int per_rank = std::max(1, p->gate_clusters[lg] / d.W);
+    const int want = (d.T + per_rank - 1) / per_rank;
+    ga.rows = std::min(kTileM, std::max(8, (want + 7) / 8 * 8));
+  }
+  for (int r = 0; r < d.W; ++r)
+    if (!aligned16(x[r]) || !make_map(p, &ga.tm_x[r], x[r], d.T, d.D, (uint32_t)ga.rows))
+      return MOE_ERR_ARG;
+  if (!make_map(p, &ga.tm_r, w_router, d.E, d.D, (uint32_t)ga.npad)) return MOE_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The routing tail fills the plan's token bitmaps (and its last CTA the counts): the
+  // bitmaps and the CTA counter start at zero.
+  const size_t z0 = p->offsets[PA_GATE_DONE];
+  const size_t z1 = p->offsets[PA_BITMAP] + p->counts[PA_BITMAP] * 4;
+  CUDA_TRY(cudaMemsetAsync(p->plan_ws + z0, 0, z1 - z0, s));
+  if (p->spans) {
+    ga.p.span = span_record(p, p->nspan);
+    CUDA_TRY(cudaMemsetAsync(ga.p.span + kSpanGateStart, 0, 2 * sizeof(unsigned long long), s));
+  }
   tstart(p, kTRoute, s);
   CUDA_TRY(launch_gate(ga, s));
   tstop(p, kTRoute, s);
+  p->gate_counted = true;
+  p->gate_ids = ids;
   return MOE_OK;
 }
 
 int moe_plan_build(moe_plan* p, const int32_t* ids, const void* const* x, moe_stream_t stream) {
-  if (p == nullptr || !aligned16(ids) || x == nullptr) return MOE_ERR_ARG;
+  if (p == nullptr || x == nullptr) return MOE_ERR_ARG;
+  // ids == NULL: the routing of the last moe_gate, whose bitmaps and counts are
+  // already in the plan.
+  const bool counted = ids == nullptr;
+  if (counted) {
+    if (!p->gate_counted) return MOE_ERR_ARG;
+    ids = p->gate_ids;
+  }
+  if (!aligned16(ids)) return MOE_ERR_ARG;
   for (int r = 0; r < p->d.W; ++r)
     if (!aligned16(x[r])) return MOE_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const DevPlan dp = dev_plan(p);
   tstart(p, kTPlan, s);
-  CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_BITMAP], 0, p->counts[PA_BITMAP] * 4, s));
-  CUDA_TRY(launch_plan(dp, ids, s));
+  if (!counted)
+    CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_BITMAP], 0, p->counts[PA_BITMAP] * 4, s));
+  CUDA_TRY(launch_plan(dp, ids, s, counted));
+  p->gate_counted = false;
   const __nv_bfloat16* xs[MOE_MAX_RANKS] = {};
   __nv_bfloat16* xb[MOE_MAX_RANKS] = {};
   for (int r = 0; r < p->d.W; ++r) {
@@ -447,7 +481,7 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
   if (p->spans) {  // the kernels fold their device-clock stamps into a zeroed ring record
     pa.p.span = span_record(p, p->nspan);
     pa.p.chunk_t = reinterpret_cast<unsigned long long*>(p->plan_ws + p->offsets[PA_CHUNK_T]);
-    CUDA_TRY(cudaMemsetAsync(pa.p.span, 0, kSpanWords * sizeof(unsigned long long), sp));
+    CUDA_TRY(cudaMemsetAsync(pa.p.span, 0, kSpanCombineWords * sizeof(unsigned long long), sp));
     p->last_span = p->nspan % kSpanRing;
     p->nspan++;
   }
@@ -646,6 +680,11 @@ int moe_status_clear(moe_plan* p, moe_stream_t stream) {
 
 int moe_set_timing(moe_plan* p, int enable) {
   if (p == nullptr || enable < 0 || enable > 2) return MOE_ERR_ARG;
+  if (enable != 0) {  // start from a clean span ring (instrumentation: synchronises the device)
+    CUDA_TRY(cudaDeviceSynchronize());
+    CUDA_TRY(cudaMemset(p->plan_ws + p->offsets[PA_SPANS], 0, p->counts[PA_SPANS] * 4));
+    CUDA_TRY(cudaDeviceSynchronize());
+  }
   p->timing = enable == 1;
   p->spans = enable != 0;
   for (int i = 0; i < kTSlots; ++i) p->nrec[i] = 0;
@@ -672,7 +711,7 @@ int moe_timings(moe_plan* p, float* ms, int n) {
   }
   // Device-clock records: [6] the producer's span, [7] the overlapped scale's span,
   // [8] the part of that span before the producer's end (means over the records).
-  for (int i = kTSlots; i < n && i < kTSlots + 3; ++i) ms[i] = -1.f;
+  for (int i = kTSlots; i < n && i < kTSlots + 4; ++i) ms[i] = -1.f;
   const int m = std::min(p->nspan, kSpanRing);
   if (n > kTSlots && m > 0) {
     CUDA_TRY(cudaDeviceSynchronize());
@@ -695,6 +734,28 @@ int moe_timings(moe_plan* p, float* ms, int n) {
     ms[kTSlots] = (float)(prod / m);
     if (nscale > 0 && n > kTSlots + 1) ms[kTSlots + 1] = (float)(scale / nscale);
     if (nscale > 0 && n > kTSlots + 2) ms[kTSlots + 2] = (float)(beside / nscale);
+  }
+  // [9] the gate's span (first CTA start to last CTA end), over the records that hold one;
+  // the record a gate writes is that of the combine that follows it.
+  if (n > kTSlots + 3) {
+    ms[kTSlots + 3] = -1.f;
+    const int mg = std::min(p->nspan + 1, kSpanRing);
+    if (p->spans && mg > 0) {
+      CUDA_TRY(cudaDeviceSynchronize());
+      unsigned long long ring[kSpanWords * kSpanRing];
+      CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
+                          cudaMemcpyDeviceToHost));
+      double gate = 0.0;
+      int ngate = 0;
+      for (int j = 0; j < mg; ++j) {
+        const unsigned long long* r = ring + (size_t)kSpanWords * ((p->nspan - j) % kSpanRing);
+        if (r[kSpanGateEnd] != 0 && r[kSpanGateStart] != 0) {
+          gate += (double)(r[kSpanGateEnd] - ~r[kSpanGateStart]) * 1e-6;
+          ++ngate;
+        }
+      }
+      if (ngate > 0) ms[kTSlots + 3] = (float)(gate / ngate);
+    }
   }
   return MOE_OK;
 }

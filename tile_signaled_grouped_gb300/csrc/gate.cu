@@ -81,7 +81,31 @@ struct GSmem {
   alignas(8) uint64_t done;
   uint32_t tmem;
   int abort;
+  int last;  // this CTA finished last: it counts the token bitmaps
 };
+
+// The plan's token bitmap (TileMoE notes section 4.2: rows are grouped by expert and
+// source rank, in source-token order): one bit per (expert, source rank, token), set
+// for every routing slot of token t of rank s; an id out of range or repeated within
+// the token is reported (MOE_DEV_ROUTING) and skipped, as the plan build does. G = 1:
+// this thread routed the token; G = 32: lane j < k wrote slot j.
+template <int G>
+__device__ __forceinline__ void mark_token(const GateArgs& a, const Dims& d, size_t tok, int s,
+                                           int t, int lig, uint32_t* status) {
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(a.p.a[PA_BITMAP]);
+  const int32_t* row = a.ids + tok * d.k;
+  if (G > 1) __syncwarp();  // the ids the other lanes wrote
+  for (int j = G > 1 ? lig : 0; j < d.k; j += G) {
+    const int e = row[j];
+    bool ok = e >= 0 && e < d.E;
+    for (int q = 0; q < j && ok; ++q) ok = row[q] != e;
+    if (!ok) {
+      report_error(status, MOE_DEV_ROUTING, (uint32_t)tok);
+      continue;
+    }
+    atomicOr(&bitmap[((size_t)e * d.W + s) * d.TW + (t >> 5)], 1u << (t & 31));
+  }
+}
 
 template <int G, int PER>
 __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_constant__ GateArgs a) {
@@ -95,13 +119,15 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
   const int npad = a.npad;
   const int crank = (int)(blockIdx.x % (unsigned)C);  // cluster dims (C, 1, 1)
   const int tile = (int)(blockIdx.x / (unsigned)C);
-  const int tpr = (d.T + kTileM - 1) / kTileM;
+  const int rows = a.rows;  // tokens of this tile (the MMA computes 128 rows; the rest is void)
+  const int tpr = (d.T + rows - 1) / rows;
   const int s = tile / tpr;
-  const int t0 = (tile % tpr) * kTileM;
+  const int t0 = (tile % tpr) * rows;
   const int nk = d.D / kBlockK;
   const int kb0 = crank * nk / C, kb1 = (crank + 1) * nk / C;
   const int nkl = kb1 - kb0;
   const uint32_t stage_bytes = gate_stage_bytes(npad);
+  const uint32_t tx_bytes = (uint32_t)rows * kBlockK * 2 + (uint32_t)npad * kBlockK * 2;
   const int S = gate_stages(npad);
   const uint32_t ncols = gate_tmem_cols(npad);
   uint32_t* status = reinterpret_cast<uint32_t*>(a.p.a[PA_STATUS]);
@@ -114,6 +140,8 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
     }
     mbar_init(&sm.done, 1);
     sm.abort = 0;
+    sm.last = 0;
+    span_begin(a.p.span, kSpanGateStart);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(&sm.tmem, ncols);
@@ -133,7 +161,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
                              status, 0x50000000u))
         break;
       uint8_t* As = base + (size_t)st * stage_bytes;
-      mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
+      mbar_arrive_expect_tx(&sm.full[st], tx_bytes);
       const int kx = (kb0 + i) * kBlockK;
       tma_load_2d(As, &a.tm_x[s], &sm.full[st], kx, t0);
       tma_load_2d(As + kGateABytes, &a.tm_r, &sm.full[st], kx, 0);
@@ -200,7 +228,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
     tmem_dealloc(tmem, ncols);
   }
 
-  const int R = kTileM / C;  // rows this CTA routes: [crank * R, crank * R + R)
+  const int R = rows / C;  // rows this CTA routes: [crank * R, crank * R + R)
   const uint32_t stride = gate_part_stride(npad);
   float* part = reinterpret_cast<float*>(base);
   if (C > 1) {
@@ -253,8 +281,44 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
       }
       route_group<G, PER>(v, d.E, d.k, a.forced != nullptr ? a.forced + tok * d.k : nullptr,
                           a.ids + tok * d.k, a.w + tok * d.k, lig);
+      mark_token<G>(a, d, tok, s, t, lig, status);
     }
   }
+
+  // ------------------------------------------------------------ plan counts
+  // The CTA that finishes last turns the token bitmaps into the plan's group sizes
+  // (expert, source rank) and per-word popcount prefixes, which the plan build would
+  // otherwise compute in two kernels of its own. The counter was zeroed with the
+  // bitmaps before this launch.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sm.last = atomicAdd(reinterpret_cast<uint32_t*>(a.p.a[PA_GATE_DONE]), 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (sm.last) {
+    __threadfence();
+    const uint32_t* bitmap = reinterpret_cast<const uint32_t*>(a.p.a[PA_BITMAP]);
+    int32_t* wpre = a.p.a[PA_WPRE];
+    for (int g = warp; g < d.E * d.W; g += kGateThreads / 32) {
+      const size_t gb = (size_t)g * d.TW;
+      int carry = 0;
+      for (int w0 = 0; w0 < d.TW; w0 += 32) {
+        const int wi = w0 + lane;
+        const int c = wi < d.TW ? __popc(__ldcg(bitmap + gb + wi)) : 0;
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (wi < d.TW) wpre[gb + wi] = carry + x - c;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) a.p.a[PA_CNT][g] = carry;
+    }
+  }
+  if (threadIdx.x == 0) span_end(a.p.span, kSpanGateEnd);
 }
 
 template <int G, int PER>
@@ -327,7 +391,7 @@ int gate_clusters(int E, int splits) {
 
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s) {
   const Dims& d = a.p.d;
-  const int tiles = d.W * ((d.T + kTileM - 1) / kTileM);
+  const int tiles = d.W * ((d.T + a.rows - 1) / a.rows);
 #define MOE_GATE_LAUNCH(G, PER) launch_gate_gp<G, PER>(a, tiles, s)
   return MOE_GATE_DISPATCH(d.E, MOE_GATE_LAUNCH);
 #undef MOE_GATE_LAUNCH

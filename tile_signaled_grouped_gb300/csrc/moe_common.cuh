@@ -38,6 +38,9 @@ enum SpanWord {
   kSpanScaleStart = 2,  // ~(first CTA start) of the overlapped scale
   kSpanScaleEnd = 3,    // last CTA end of the overlapped scale
   kSpanLastTile = 4,    // the producer's last finished output tile (its ready-flag release)
+  kSpanGateStart = 5,   // ~(first CTA start) of the gate before this combine
+  kSpanGateEnd = 6,     // last CTA end of that gate
+  kSpanCombineWords = 5,  // words [0, 5) are zeroed by each combine, [5, 7) by each gate
   kSpanWords = 8
 };
 
@@ -62,7 +65,9 @@ enum PlanArray {
   PA_STATUS = 0, PA_TOTALS,
   // zeroed at the start of every combine (one memset):
   PA_QUEUE, PA_G1CNT, PA_FLAGS, PA_GROUP_DONE, PA_GROUP_SIG,
-  // zeroed at the start of every plan build:
+  // zeroed at the start of every plan build (and of every gate, whose routing tail
+  // fills them):
+  PA_GATE_DONE,  // [4] [0]: gate CTAs finished (the last one counts the bitmaps)
   PA_BITMAP,
   // plain arrays:
   PA_WPRE, PA_CNT, PA_GROUP_START, PA_RECV_OFF,
@@ -120,7 +125,9 @@ cudaError_t preload_plan();
 cudaError_t preload_route_scale();
 cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* forced,
                          int32_t* ids, float* w, cudaStream_t s);
-cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s);
+// counted: the token bitmaps, group sizes and word prefixes are already in the plan
+// (the gate's routing tail wrote them), so the first two plan kernels are skipped.
+cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s, bool counted = false);
 cudaError_t launch_gather(const DevPlan& p, const __nv_bfloat16* const* x,
                           __nv_bfloat16* const* xbuf, int num_sms, cudaStream_t s);
 
@@ -136,6 +143,7 @@ struct GateArgs {
   DevPlan p;
   int npad;    // MMA N: E rounded up to 32
   int splits;  // CTAs of one cluster sharing a token tile, each summing a K range
+  int rows;    // tokens per tile: a multiple of 8, at most 128 (the x maps' box height)
 };
 cudaError_t preload_gate();
 // Clusters of `splits` CTAs (1, 2, 4 or 8) resident at once on an idle GPU, for E

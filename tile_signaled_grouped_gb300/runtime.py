@@ -86,7 +86,12 @@ class ExpertCombine:
                       _stream_handle(stream))
         return self.ids, self.w
 
-    def plan_build(self, x, ids=None, stream=None):
+    def plan_build(self, x, ids=None, stream=None, from_gate=False):
+        """from_gate: build from the routing of the last gate() call, whose routing
+        tail already wrote the plan's token bitmaps and counts (two plan kernels fewer)."""
+        if from_gate:
+            capi.moe_plan_build(self.plan, None, [t.data_ptr() for t in x], _stream_handle(stream))
+            return
         ids = self.ids if ids is None else ids
         capi.moe_plan_build(self.plan, ids.data_ptr(), [t.data_ptr() for t in x],
                             _stream_handle(stream))
@@ -135,7 +140,7 @@ class ExpertCombine:
             self.gate(x, w_router, forced_ids, producer)
         else:
             self.route(logits, forced_ids, producer)
-        self.plan_build(x, stream=producer)
+        self.plan_build(x, stream=producer, from_gate=w_router is not None)
         self.expert_combine(w_gate, w_up, w_down, producer, consumer)
         return self.scale_step(stream=producer, out=out)
 
@@ -222,8 +227,9 @@ class ExpertCombine:
 
     def timings(self):
         """[route or gate, plan, producer, consumer, scale, gather, producer span,
-        gated-scale span, gated-scale time before the producer's end] in ms (-1: none)."""
-        return capi.moe_timings(self.plan, 9)
+        gated-scale span, gated-scale time before the producer's end, gate span] in ms
+        (-1: none)."""
+        return capi.moe_timings(self.plan, 10)
 
     def combine_overlap(self):
         """(share of the combine's bytes landed before the producer's last tile, µs from
@@ -308,7 +314,7 @@ class HostPipeline:
             lay.gate(self.x[b], w_router, fid, sp)
         else:
             lay.route(self.logits[b], fid, sp)
-        lay.plan_build(self.x[b], stream=sp)
+        lay.plan_build(self.x[b], stream=sp, from_gate=w_router is not None)
         self.ev_free[b].record(sp)
         # The output set is rewritten only after its previous copy to the host; the wait
         # comes before the combine, so nothing separates the combine from the scale.
