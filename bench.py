@@ -172,7 +172,7 @@ def gpu_arm(args, rank, world, local_rank):
     inp = make_inputs(wl, device="cuda")
     # --route gate: every step routes from the token rows with the gate kernel (router
     # scores, softmax and top-k in one launch; a prescribed routing keeps its ids), and
-    # the plan starts from the counts the gate's routing tail wrote.
+    # the plan starts from the token bitmaps the gate's routing tail set.
     wr = None
     if args.route == "gate":
         from tile_signaled_grouped_gb300.workloads import router_weights
@@ -326,8 +326,8 @@ def gpu_arm(args, rank, world, local_rank):
                      "per_step_source": "executed FLOPs of one step / ms_per_step"},
         "e2e": e2e,
         # route 1 + plan 5 + gather 1 + producer 1 + scale 1, + consumer kernel 1 unless
-        # fused; routed by the gate: gate 1 + plan 3 (the gate wrote the counts)
-        "gpu_launches": ((9 if wr is None else 7) + (0 if args.consumer_ctas < 0 else 1))
+        # fused; routed by the gate: gate 1 + plan 4 (the gate set the token bitmaps)
+        "gpu_launches": ((9 if wr is None else 8) + (0 if args.consumer_ctas < 0 else 1))
         * args.steps,
         "clocks": clk.summary(),
         "stages": stages,
@@ -722,7 +722,7 @@ def main():
     ap.add_argument("--route", default="logits", choices=["logits", "gate"],
                     help="logits: route from the drawn gate logits; gate: the gate kernel scores "
                          "the token rows with a seeded router (softmax and top-k in the same "
-                         "launch) and writes the plan's counts")
+                         "launch) and sets the plan's token bitmaps")
     ap.add_argument("--producer-pairs", type=int, default=1, choices=[0, 1],
                     help="1: the CTA-pair producer (clusters of two, tcgen05 cta_group::2)")
     ap.add_argument("--gate-only", action="store_true",

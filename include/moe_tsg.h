@@ -136,9 +136,8 @@ int moe_route(moe_plan *plan, const float *logits, const int32_t *forced_ids,
  *              partial sums are added in a fixed order, so a given split gives
  *              the same bits on every call).
  * Each tile holds as many tokens (a multiple of 8, at most 128) as fill one wave of
- * CTAs. The routing tail also writes the plan's token bitmaps, and the CTA that
- * finishes last the group sizes and word prefixes (ids out of range or repeated set
- * MOE_DEV_ROUTING), for a following moe_plan_build(plan, NULL, ...).
+ * CTAs. The routing tail also sets the plan's token bitmaps (prescribed ids out of
+ * range or repeated set MOE_DEV_ROUTING), for a following moe_plan_build(plan, NULL, ...).
  * E <= 256; larger E, or a split the GPU cannot hold, gives MOE_ERR_UNSUPPORTED.
  * The caller owns every buffer. Timed in slot [0] of moe_timings, its device-clock
  * span in slot [9]. */
@@ -151,8 +150,8 @@ int moe_gate(moe_plan *plan, const void *const *x, const void *w_router,
  * owner's expert input X with its tokens' rows (zero rows for padding).
  *  topk_ids: [W][T][topk] int32, ids distinct within a token; or NULL: the routing of
  *            the last moe_gate on this plan (no moe_route or moe_plan_build since),
- *            whose routing tail already wrote the token bitmaps and group counts, so
- *            two plan kernels are skipped; MOE_ERR_ARG if there is none.
+ *            whose routing tail already set the plan's token bitmaps, so the bitmap
+ *            kernel is skipped; MOE_ERR_ARG if there is none.
  *  x:        W pointers, rank s's tokens [T][D] bf16.
  * Ids out of range or repeated set MOE_DEV_ROUTING; the offending assignments are
  * skipped. No device-to-host transfer: every size is read on the device. */

@@ -263,10 +263,9 @@ def test_captured_step_from_the_router_replays_bit_exactly():
                                 get_workload("qwen3_235b_like", routing="gate"),
                                 get_workload("a100_like")], ids=lambda w: w.name)
 def test_gate_writes_the_plan_counts(wl, splits):
-    """The gate's routing tail sets the plan's token bitmaps and its last CTA the group
-    sizes and word prefixes: the plan built from them (moe_plan_build with NULL ids, two
-    plan kernels fewer) equals, array for array, the plan the plan kernels build from
-    the same ids."""
+    """The gate's routing tail sets the plan's token bitmaps: the plan built from them
+    (moe_plan_build with NULL ids, no bitmap kernel) equals, array for array, the plan
+    the plan kernels build from the same ids."""
     inp = make_inputs(wl, device="cuda", with_weights=False)
     wr = router_weights(wl, device="cuda")
     layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb)

@@ -46,7 +46,7 @@ struct moe_plan {
   bool timing;        // CUDA events around each kernel
   bool spans;         // device-clock records (span ring, chunk landing stamps)
   bool gated_armed;   // a combine was enqueued since the last moe_scale_gated
-  bool gate_counted;  // the last routing call was moe_gate: its bitmaps and counts are in the plan
+  bool gate_marked;   // the last routing call was moe_gate: its token bitmaps are in the plan
   const int32_t* gate_ids;  // the ids that moe_gate wrote
 };
 
@@ -109,7 +109,6 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_FLAGS] = W * NBM * d.nt2;
   n[PA_GROUP_DONE] = W * W;
   n[PA_GROUP_SIG] = W * W;
-  n[PA_GATE_DONE] = 4;
   n[PA_BITMAP] = E * W * d.TW;
   n[PA_WPRE] = E * W * d.TW;
   n[PA_CNT] = n[PA_GROUP_START] = n[PA_RECV_OFF] = E * W;
@@ -362,7 +361,7 @@ int moe_route(moe_plan* p, const float* logits, const int32_t* forced, int32_t* 
   tstart(p, kTRoute, s);
   CUDA_TRY(launch_route(dp, logits, forced, ids, w, s));
   tstop(p, kTRoute, s);
-  p->gate_counted = false;
+  p->gate_marked = false;
   return MOE_OK;
 }
 
@@ -405,11 +404,8 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
       return MOE_ERR_ARG;
   if (!make_map(p, &ga.tm_r, w_router, d.E, d.D, (uint32_t)ga.npad)) return MOE_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The routing tail fills the plan's token bitmaps (and its last CTA the counts): the
-  // bitmaps and the CTA counter start at zero.
-  const size_t z0 = p->offsets[PA_GATE_DONE];
-  const size_t z1 = p->offsets[PA_BITMAP] + p->counts[PA_BITMAP] * 4;
-  CUDA_TRY(cudaMemsetAsync(p->plan_ws + z0, 0, z1 - z0, s));
+  // The routing tail sets the plan's token bitmaps: they start at zero.
+  CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_BITMAP], 0, p->counts[PA_BITMAP] * 4, s));
   if (p->spans) {
     ga.p.span = span_record(p, p->nspan);
     CUDA_TRY(cudaMemsetAsync(ga.p.span + kSpanGateStart, 0, 2 * sizeof(unsigned long long), s));
@@ -417,18 +413,18 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
   tstart(p, kTRoute, s);
   CUDA_TRY(launch_gate(ga, s));
   tstop(p, kTRoute, s);
-  p->gate_counted = true;
+  p->gate_marked = true;
   p->gate_ids = ids;
   return MOE_OK;
 }
 
 int moe_plan_build(moe_plan* p, const int32_t* ids, const void* const* x, moe_stream_t stream) {
   if (p == nullptr || x == nullptr) return MOE_ERR_ARG;
-  // ids == NULL: the routing of the last moe_gate, whose bitmaps and counts are
-  // already in the plan.
-  const bool counted = ids == nullptr;
-  if (counted) {
-    if (!p->gate_counted) return MOE_ERR_ARG;
+  // ids == NULL: the routing of the last moe_gate, whose token bitmaps are already
+  // in the plan.
+  const bool marked = ids == nullptr;
+  if (marked) {
+    if (!p->gate_marked) return MOE_ERR_ARG;
     ids = p->gate_ids;
   }
   if (!aligned16(ids)) return MOE_ERR_ARG;
@@ -437,10 +433,10 @@ int moe_plan_build(moe_plan* p, const int32_t* ids, const void* const* x, moe_st
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const DevPlan dp = dev_plan(p);
   tstart(p, kTPlan, s);
-  if (!counted)
+  if (!marked)
     CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_BITMAP], 0, p->counts[PA_BITMAP] * 4, s));
-  CUDA_TRY(launch_plan(dp, ids, s, counted));
-  p->gate_counted = false;
+  CUDA_TRY(launch_plan(dp, ids, s, marked));
+  p->gate_marked = false;
   const __nv_bfloat16* xs[MOE_MAX_RANKS] = {};
   __nv_bfloat16* xb[MOE_MAX_RANKS] = {};
   for (int r = 0; r < p->d.W; ++r) {

@@ -81,27 +81,32 @@ struct GSmem {
   alignas(8) uint64_t done;
   uint32_t tmem;
   int abort;
-  int last;  // this CTA finished last: it counts the token bitmaps
 };
 
 // The plan's token bitmap (TileMoE notes section 4.2: rows are grouped by expert and
 // source rank, in source-token order): one bit per (expert, source rank, token), set
-// for every routing slot of token t of rank s; an id out of range or repeated within
-// the token is reported (MOE_DEV_ROUTING) and skipped, as the plan build does. G = 1:
-// this thread routed the token; G = 32: lane j < k wrote slot j.
+// for every routing slot of token t of rank s, so that the plan build after a gate
+// skips its bitmap kernel (the group counts stay in the plan's count kernel, which,
+// unlike this kernel, fits beside a running producer CTA). G = 1: this thread routed the token;
+// G = 32: lane j < k wrote slot j. The gate's own top k is k distinct ids in range;
+// prescribed ids are checked like the plan build checks them (out of range or
+// repeated within the token: MOE_DEV_ROUTING, the slot skipped).
 template <int G>
 __device__ __forceinline__ void mark_token(const GateArgs& a, const Dims& d, size_t tok, int s,
                                            int t, int lig, uint32_t* status) {
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(a.p.a[PA_BITMAP]);
   const int32_t* row = a.ids + tok * d.k;
-  if (G > 1) __syncwarp();  // the ids the other lanes wrote
+  const bool check = a.forced != nullptr;
+  if (G > 1 && check) __syncwarp();  // the ids the other lanes wrote
   for (int j = G > 1 ? lig : 0; j < d.k; j += G) {
     const int e = row[j];
-    bool ok = e >= 0 && e < d.E;
-    for (int q = 0; q < j && ok; ++q) ok = row[q] != e;
-    if (!ok) {
-      report_error(status, MOE_DEV_ROUTING, (uint32_t)tok);
-      continue;
+    if (check) {
+      bool ok = e >= 0 && e < d.E;
+      for (int q = 0; q < j && ok; ++q) ok = row[q] != e;
+      if (!ok) {
+        report_error(status, MOE_DEV_ROUTING, (uint32_t)tok);
+        continue;
+      }
     }
     atomicOr(&bitmap[((size_t)e * d.W + s) * d.TW + (t >> 5)], 1u << (t & 31));
   }
@@ -133,6 +138,9 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
   uint32_t* status = reinterpret_cast<uint32_t*>(a.p.a[PA_STATUS]);
   const long long itimeout = a.p.timeout_ns + 4000000000LL;
 
+  // The TMA thread initialises the barriers and issues the first S stages' loads at
+  // once (every stage starts free), before the CTA waits for its TMEM allocation.
+  const int early = nkl < S ? nkl : S;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&sm.full[i], 1);
@@ -140,11 +148,19 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
     }
     mbar_init(&sm.done, 1);
     sm.abort = 0;
-    sm.last = 0;
     span_begin(a.p.span, kSpanGateStart);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&a.tm_x[s]);
+    tma_prefetch_desc(&a.tm_r);
+    for (int i = 0; i < early; ++i) {
+      uint8_t* As = base + (size_t)i * stage_bytes;
+      mbar_arrive_expect_tx(&sm.full[i], tx_bytes);
+      const int kx = (kb0 + i) * kBlockK;
+      tma_load_2d(As, &a.tm_x[s], &sm.full[i], kx, t0);
+      tma_load_2d(As + kGateABytes, &a.tm_r, &sm.full[i], kx, 0);
+    }
   }
-  if (warp == 0) tmem_alloc(&sm.tmem, ncols);
+  if (warp == 1) tmem_alloc(&sm.tmem, ncols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -152,9 +168,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA
-    tma_prefetch_desc(&a.tm_x[s]);
-    tma_prefetch_desc(&a.tm_r);
-    int i = 0;
+    int i = early;
     for (; i < nkl; ++i) {
       const int st = i % S;
       if (!mbar_wait_bounded(&sm.empty[st], ((i / S) & 1) ^ 1, &sm.abort, itimeout,
@@ -223,7 +237,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
   __syncwarp();
   cluster_sync_all();  // every CTA's partial sums are in its shared memory
   tc_fence_after();
-  if (warp == 0) {
+  if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem, ncols);
   }
@@ -285,39 +299,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
     }
   }
 
-  // ------------------------------------------------------------ plan counts
-  // The CTA that finishes last turns the token bitmaps into the plan's group sizes
-  // (expert, source rank) and per-word popcount prefixes, which the plan build would
-  // otherwise compute in two kernels of its own. The counter was zeroed with the
-  // bitmaps before this launch.
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    sm.last = atomicAdd(reinterpret_cast<uint32_t*>(a.p.a[PA_GATE_DONE]), 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (sm.last) {
-    __threadfence();
-    const uint32_t* bitmap = reinterpret_cast<const uint32_t*>(a.p.a[PA_BITMAP]);
-    int32_t* wpre = a.p.a[PA_WPRE];
-    for (int g = warp; g < d.E * d.W; g += kGateThreads / 32) {
-      const size_t gb = (size_t)g * d.TW;
-      int carry = 0;
-      for (int w0 = 0; w0 < d.TW; w0 += 32) {
-        const int wi = w0 + lane;
-        const int c = wi < d.TW ? __popc(__ldcg(bitmap + gb + wi)) : 0;
-        int x = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (wi < d.TW) wpre[gb + wi] = carry + x - c;
-        carry += __shfl_sync(0xffffffffu, x, 31);
-      }
-      if (lane == 0) a.p.a[PA_CNT][g] = carry;
-    }
-  }
   if (threadIdx.x == 0) span_end(a.p.span, kSpanGateEnd);
 }
 

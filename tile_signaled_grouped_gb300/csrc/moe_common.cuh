@@ -66,8 +66,7 @@ enum PlanArray {
   // zeroed at the start of every combine (one memset):
   PA_QUEUE, PA_G1CNT, PA_FLAGS, PA_GROUP_DONE, PA_GROUP_SIG,
   // zeroed at the start of every plan build (and of every gate, whose routing tail
-  // fills them):
-  PA_GATE_DONE,  // [4] [0]: gate CTAs finished (the last one counts the bitmaps)
+  // fills it):
   PA_BITMAP,
   // plain arrays:
   PA_WPRE, PA_CNT, PA_GROUP_START, PA_RECV_OFF,
@@ -125,9 +124,9 @@ cudaError_t preload_plan();
 cudaError_t preload_route_scale();
 cudaError_t launch_route(const DevPlan& p, const float* logits, const int32_t* forced,
                          int32_t* ids, float* w, cudaStream_t s);
-// counted: the token bitmaps, group sizes and word prefixes are already in the plan
-// (the gate's routing tail wrote them), so the first two plan kernels are skipped.
-cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s, bool counted = false);
+// marked: the token bitmaps are already in the plan (the gate's routing tail set
+// them), so the bitmap kernel is skipped.
+cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s, bool marked = false);
 cudaError_t launch_gather(const DevPlan& p, const __nv_bfloat16* const* x,
                           __nv_bfloat16* const* xbuf, int num_sms, cudaStream_t s);
 

@@ -665,14 +665,14 @@ cudaError_t preload_plan() {
   return cudaFuncGetAttributes(&fa, layout_gather_kernel);
 }
 
-cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s, bool counted) {
+cudaError_t launch_plan(const DevPlan& p, const int32_t* ids, cudaStream_t s, bool marked) {
   const Dims& d = p.d;
-  if (!counted) {
+  if (!marked) {
     const int ntok = d.W * d.T;
     plan_bitmap_kernel<<<(ntok + 255) / 256, 256, 0, s>>>(p, ids);
-    const int warps = d.E * d.W;
-    plan_count_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
   }
+  const int warps = d.E * d.W;
+  plan_count_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
   plan_rank_kernel<<<d.W, kPlanThreads, rank_smem_bytes(d.L, d.W), s>>>(p);
   const int na = d.W * d.T * d.k;
   plan_scatter_kernel<<<(na + 255) / 256, 256, 0, s>>>(p, ids);

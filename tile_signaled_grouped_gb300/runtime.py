@@ -88,7 +88,7 @@ class ExpertCombine:
 
     def plan_build(self, x, ids=None, stream=None, from_gate=False):
         """from_gate: build from the routing of the last gate() call, whose routing
-        tail already wrote the plan's token bitmaps and counts (two plan kernels fewer)."""
+        tail already set the plan's token bitmaps (one plan kernel fewer)."""
         if from_gate:
             capi.moe_plan_build(self.plan, None, [t.data_ptr() for t in x], _stream_handle(stream))
             return
