@@ -257,15 +257,17 @@ def gpu_arm(args, rank, world, local_rank):
 
     # ---- e2e through the C ABI with host buffers, right after the timed region (the
     # same power state: the GPU sits at its power cap within a fraction of a second) ---
-    e2e = e2e_arm(layers, inp, wl, sp, sc, args, wr)
+    e2e = e2e_arm(layers, inp, wl, sp, sc, args, wr) if not args.no_e2e else None
 
     # ---- stage measurements (outside the timed region) --------------------------------
     # They time kernels one at a time against the burst peaks, so they start from a
     # rested GPU: after the timed region and the e2e leg the power limiter holds the
     # clocks down for a while, and a few idle seconds release it.
-    torch.cuda.synchronize()
-    time.sleep(3.0)
-    stages = stage_times(layer, inp, wl, sp, sc, args)
+    stages = None
+    if not args.no_stages:
+        torch.cuda.synchronize()
+        time.sleep(3.0)
+        stages = stage_times(layer, inp, wl, sp, sc, args)
 
     hbm, bf16, bf16_sus, src = _peaks()
     launch = layer.launch_info()
@@ -712,6 +714,11 @@ def main():
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stages", action="store_true",
+                    help="skip the per-kernel stage measurements and schedule sweeps (short "
+                         "runs, e.g. under a profiler)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg through host buffers")
     ap.add_argument("--batches-in-flight", type=int, default=2,
                     help="layer instances (own plan and workspaces) that take steps in turn, so "
                          "one batch's routing, plan and gather overlap the previous batch's FFN")
