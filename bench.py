@@ -346,11 +346,83 @@ def gpu_arm(args, rank, world, local_rank):
         "combine_overlap": {"landed_before_last_tile": landed, "last_copy_after_last_tile_us": tail_us,
                             "copy_bytes": copy_bytes},
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     for lay in layers:
         lay.close()
+    del layers, inp
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if not args.no_other_workloads and not args.tokens_per_rank:
+        result["other_workloads"] = other_workloads(args, wl.name)
     return result
+
+
+def other_workloads(args, skip):
+    """The other workload shapes at full size, each with the bench's default schedule
+    (fused producer and copy, two batches in flight): whole-step time from CUDA events
+    over a few steps (device inputs; but for the tiny shape the expert weights are
+    larger than L2 and stream from HBM every step), the producer's device-clock span and
+    its share of the bf16 burst peak, and the combine overlap."""
+    import torch
+
+    from tile_signaled_grouped_gb300 import capi
+    from tile_signaled_grouped_gb300.runtime import ExpertCombine
+    from tile_signaled_grouped_gb300.workloads import WORKLOADS, make_inputs
+
+    _, bf16, _, src = _peaks()
+    out = {}
+    for name, wl in WORKLOADS.items():
+        if name == skip:
+            continue
+        inp = make_inputs(wl, device="cuda")
+        torch.cuda.synchronize()
+        lays = [ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb,
+                              args.consumer_ctas, producer_pairs=args.producer_pairs,
+                              scale_mode=args.scale) for _ in range(2)]
+        sps = [torch.cuda.Stream(), torch.cuda.Stream()]
+        scs = [torch.cuda.Stream(priority=-1), torch.cuda.Stream(priority=-1)]
+
+        def run(i):
+            lays[i % 2].forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits,
+                                inp.forced_ids, producer=sps[i % 2], consumer=scs[i % 2])
+
+        for i in range(4):
+            run(i)
+        torch.cuda.synchronize()
+        steps = 10
+        lays[0].set_timing(2)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(sps[0])
+        sps[1].wait_event(ev0)
+        for i in range(steps):
+            run(i)
+        sps[0].wait_stream(sps[1])
+        ev1.record(sps[0])
+        torch.cuda.synchronize()
+        for lay in lays:
+            if lay.status() != (0, 0):
+                raise RuntimeError(f"device status {lay.status()} on {name}")
+        t = lays[0].timings()
+        landed, tail_us, copy_bytes = lays[0].combine_overlap()
+        rows = int(lays[0].field(capi.MOE_PLAN_RANK_ROWS).sum().item())
+        flops = 6.0 * rows * wl.d_model * wl.d_ff
+        ms = ev0.elapsed_time(ev1) / steps
+        out[name] = {
+            "ms_per_step": ms, "tokens_per_s": wl.W * wl.T / (ms * 1e-3), "steps": steps,
+            "producer_span_ms": t[6],
+            "producer_tflops": flops / (t[6] * 1e-3) / 1e12,
+            "producer_frac": flops / (t[6] * 1e-3) / 1e12 / bf16,
+            "per_step_frac": flops / (ms * 1e-3) / 1e12 / bf16,
+            "peak": f"{src} bf16 burst {bf16}",
+            "tflop_executed": flops / 1e12,
+            "tflop_valid": 6.0 * wl.W * wl.T * wl.topk * wl.d_model * wl.d_ff / 1e12,
+            "combine_landed_before_last_tile": landed,
+        }
+        for lay in lays:
+            lay.close()
+        del lays, inp
+        torch.cuda.empty_cache()
+    return out
 
 
 def measure_gate(lay, x, wl, stream, iters, warmup, hbm):
@@ -719,6 +791,8 @@ def main():
                          "runs, e.g. under a profiler)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end leg through host buffers")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the short runs of the other workload shapes")
     ap.add_argument("--batches-in-flight", type=int, default=2,
                     help="layer instances (own plan and workspaces) that take steps in turn, so "
                          "one batch's routing, plan and gather overlap the previous batch's FFN")
