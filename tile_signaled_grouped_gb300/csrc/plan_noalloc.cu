@@ -21,7 +21,7 @@ namespace {
 
 // Scratch shared by every call on a device; held by each GPU that loads the
 // library until the process exits. 1 MiB covers every workload shape of the
-// tests (the largest, a 256-expert layer, needs about 330 KB).
+// tests (the largest, a 256-expert layer, needs about 194 KB).
 constexpr size_t kScratchBytes = 1u << 20;
 static __device__ __align__(256) uint8_t g_plan_scratch[kScratchBytes];
 
