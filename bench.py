@@ -14,6 +14,7 @@ GPU), so `--gpus N` runs N independent replicas, one per GPU.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -113,14 +114,14 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
-def producer_traffic(wl_name: str, tokens_override: int, pairs: int):
+def producer_traffic(wl_name: str, reduced: bool, pairs: int):
     """DRAM bytes (read + write) per producer launch, from the committed ncu summary of the
     A100-like full-size run of the producer in use, while its sources still hash to the
     fingerprint recorded there; None otherwise (changed kernel, other workload)."""
     import hashlib
     import re
 
-    if wl_name != WORKLOAD or tokens_override:
+    if wl_name != WORKLOAD or reduced:
         return None
     summary, srcs = (("ffn_pair_a100_like.md", ("ffn_pair.cu", "combine_copy.cuh")) if pairs
                      else ("ffn_producer_a100_like.md", ("ffn.cu",)))
@@ -166,8 +167,15 @@ def gpu_arm(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     wl = get_workload(args.workload)
-    if args.tokens_per_rank:
-        wl = get_workload(args.workload, T=args.tokens_per_rank)
+    reduced = bool(args.tokens_per_rank or args.experts_per_rank)
+    if reduced:  # a smaller case of the shape (profiling): a name of its own
+        over = {}
+        if args.tokens_per_rank:
+            over["T"] = args.tokens_per_rank
+        if args.experts_per_rank:
+            over["L"] = args.experts_per_rank
+        wl = get_workload(args.workload, **over)
+        wl = dataclasses.replace(wl, name=f"{wl.name}_L{wl.L}_T{wl.T}")
     W, T, D, F, k = wl.W, wl.T, wl.d_model, wl.d_ff, wl.topk
     inp = make_inputs(wl, device="cuda")
     # --route gate: every step routes from the token rows with the gate kernel (router
@@ -318,7 +326,7 @@ def gpu_arm(args, rank, world, local_rank):
                      + "GEMM1+SiLU+GEMM2, executed rows)",
                      "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": producer_traffic(wl.name, args.tokens_per_rank, args.producer_pairs),
+                     "traffic": producer_traffic(wl.name, reduced, args.producer_pairs),
                      "peak_source": (f"{src} bf16 {peak_kind} (timed region {region_s:.3f} s; "
                                      "burst below 1 s, sustained above)"),
                      "flops_per_launch": flops_exec, "launch_ms": prod_avg,
@@ -352,7 +360,7 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    if not args.no_other_workloads and not args.tokens_per_rank:
+    if not args.no_other_workloads and not reduced:
         result["other_workloads"] = other_workloads(args, wl.name)
     return result
 
@@ -784,6 +792,8 @@ def main():
                          "the producer (two kernels, two streams)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override T of the workload (smaller cases for profiling)")
+    ap.add_argument("--experts-per-rank", type=int, default=0,
+                    help="override L of the workload (smaller cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stages", action="store_true",
