@@ -140,22 +140,23 @@ __global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ Scal
 // each (sender, destination) group). Launched right behind the producer (or the
 // consumer) on its stream as a programmatic dependent launch, so its CTAs are placed
 // only once every CTA of that kernel is resident, and run beside it. Two gates, each
-// watched by one thread per CTA with long sleeps between reads (so the waiting CTAs
-// take almost nothing from the producer): first every (sender, destination) group
-// that sends rows has signalled, which makes every receive row final; then every
-// output tile of the producer has been counted, which makes every local row final.
-// Past the first gate the warps sum the tokens whose slots are all remote (their
-// rows are in the receive buffers), while the producer still works through the local
-// tiles it schedules last; past the second, the rest. Warps claim scale_kernel's tasks
-// eight at a time from two counters of the plan (zeroed by the combine), and sum them
-// with the same rounds: the same bits.
+// watched by one thread with 1 us sleeps between reads: first every (sender,
+// destination) group that sends rows has signalled, which makes every receive row
+// final; then every output tile of the producer has been counted, which makes every
+// local row final. Past the first gate, one warp per CTA sums the tokens whose slots
+// are all remote while the producer still works through the local tiles it schedules
+// last: one warp, so that this traffic beside the producer stays small. Past the
+// second gate every warp takes what is left of those tokens, then the rest. Warps
+// claim scale_kernel's tasks eight at a time from two counters of the plan (zeroed by
+// the combine), and sum them with the same rounds: the same bits.
 constexpr int kScaleClaim = 8;
 constexpr int kGatePollNs = 1000;  // sleep between two reads of a gate
+constexpr int kScaleThreads = 256;
 
 template <int SG, int CPL>
-__global__ void __launch_bounds__(256) scale_gated_kernel(const __grid_constant__ ScaleArgs a) {
+__global__ void __launch_bounds__(kScaleThreads) scale_gated_kernel(const __grid_constant__ ScaleArgs a) {
   const Dims d = a.p.d;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n16 = d.D / 8;
   const int nblk = (n16 + 32 * CPL - 1) / (32 * CPL);
   const int ntask = d.W * d.T * nblk;
@@ -165,48 +166,39 @@ __global__ void __launch_bounds__(256) scale_gated_kernel(const __grid_constant_
   uint32_t* claim = queue + 1;  // [1], [2]: the token counters of the two passes
   const uint32_t* tiles_done = queue + 3;  // output tiles (tile, N-tile) the producer finished
   __shared__ int s_ok;
-  if (threadIdx.x == 0) {
-    span_begin(a.p.span, kSpanScaleStart);
-    s_ok = 1;
-  }
-  bool ok = true;
-  for (int pass = 0; pass < 2 && ok; ++pass) {
-    if (threadIdx.x == 0 && s_ok) {
-      // Bounded wait for this pass's gate, one read per kGatePollNs.
-      const unsigned long long t0 = globaltimer();
-      const uint32_t need = (uint32_t)a.p.a[PA_TOTALS][0] * (uint32_t)d.nt2;
-      int g = 0;
-      while (true) {
-        bool open;
-        if (pass == 0) {
-          while (g < d.W * d.W && (__ldg(a.p.a[PA_GROUP_NCHUNK] + g) == 0 ||
-                                   ld_relaxed_u32(gsig + g) != 0u))
-            ++g;
-          open = g == d.W * d.W;
-        } else {
-          open = ld_relaxed_u32(tiles_done) >= need;
-        }
-        if (open) break;
-        if (ld_relaxed_u32(status) != 0u) {
-          s_ok = 0;
-          break;
-        }
-        if ((long long)(globaltimer() - t0) > a.p.timeout_ns) {
-          report_error(status, MOE_DEV_TIMEOUT, 0x70000000u | (uint32_t)pass);
-          s_ok = 0;
-          break;
-        }
-        __nanosleep(kGatePollNs);
+  if (threadIdx.x == 0) span_begin(a.p.span, kSpanScaleStart);
+
+  // Bounded wait of one thread for a gate (0: group signals, 1: finished tiles); false
+  // when the status word is set or the wait ran out (then the status says so).
+  auto wait_gate = [&](int gate) -> bool {
+    const unsigned long long t0 = globaltimer();
+    const uint32_t need = (uint32_t)a.p.a[PA_TOTALS][0] * (uint32_t)d.nt2;
+    int g = 0;
+    while (true) {
+      bool open;
+      if (gate == 0) {
+        while (g < d.W * d.W &&
+               (__ldg(a.p.a[PA_GROUP_NCHUNK] + g) == 0 || ld_relaxed_u32(gsig + g) != 0u))
+          ++g;
+        open = g == d.W * d.W;
+      } else {
+        open = ld_relaxed_u32(tiles_done) >= need;
       }
-      fence_acq_rel_gpu();  // the reads that opened the gate become acquires
+      if (open) break;
+      if (ld_relaxed_u32(status) != 0u) return false;
+      if ((long long)(globaltimer() - t0) > a.p.timeout_ns) {
+        report_error(status, MOE_DEV_TIMEOUT, 0x70000000u | (uint32_t)gate);
+        return false;
+      }
+      __nanosleep(kGatePollNs);
     }
-    __syncthreads();
-    ok = s_ok != 0;
-    if (!ok) break;
-    fence_acq_rel_gpu();
-    // Tasks as in scale_kernel (one round of one token), claimed kScaleClaim at a
-    // time; a task whose token belongs to the other pass is skipped. The next task's
-    // sources and weights are fetched while the current one is summed.
+    fence_acq_rel_gpu();  // the reads that opened the gate become acquires
+    return true;
+  };
+  // One warp takes tasks of a pass (one round of one token each, as in scale_kernel),
+  // kScaleClaim at a time, skipping tasks whose token belongs to the other pass; the
+  // next task's sources and weights are fetched while the current one is summed.
+  auto run_pass = [&](int pass) {
     int task = 0, end = 0;
     int src_n = INT_MIN;
     float w_n = 0.f;
@@ -235,6 +227,26 @@ __global__ void __launch_bounds__(256) scale_gated_kernel(const __grid_constant_
       if (__any_sync(0xffffffffu, local) != (pass == 1)) continue;
       scale_round<SG, CPL, true>(a, d, tok / d.T, tok % d.T, src, wt, lane, c0);
     }
+  };
+
+  bool ok;
+  if (warp == 0) {
+    // The early warp: both gates itself, the all-remote tokens in between.
+    ok = __shfl_sync(0xffffffffu, lane == 0 ? (wait_gate(0) ? 1 : 0) : 0, 0) != 0;
+    fence_acq_rel_gpu();
+    if (ok) run_pass(0);
+    if (ok) ok = __shfl_sync(0xffffffffu, lane == 0 ? (wait_gate(1) ? 1 : 0) : 0, 0) != 0;
+    fence_acq_rel_gpu();
+  } else {
+    // The other warps: one thread waits for both gates, then a barrier of these warps.
+    if (threadIdx.x == 32) s_ok = wait_gate(0) && wait_gate(1) ? 1 : 0;
+    asm volatile("bar.sync 1, %0;" ::"n"(kScaleThreads - 32) : "memory");
+    ok = s_ok != 0;
+    fence_acq_rel_gpu();
+  }
+  if (ok) {
+    run_pass(0);  // what the early warps left of the all-remote tokens
+    run_pass(1);
   }
   __syncthreads();
   if (threadIdx.x == 0) span_end(a.p.span, kSpanScaleEnd);
