@@ -198,7 +198,7 @@ int moe_scale(moe_plan *plan, const float *topk_w, const void *const *recv, void
  * between the combine and this call on the stream (an event, a wait) makes it start
  * after the combine instead, with the same results. Waits are bounded by timeout_ns
  * (MOE_DEV_TIMEOUT); a status already set makes the kernel return. One call per
- * moe_expert_combine (MOE_ERR_ARG otherwise). No CUDA events are recorded around it
+ * moe_expert_combine, on its producer stream (MOE_ERR_ARG otherwise). No CUDA events are recorded around it
  * (they would keep it from overlapping); with moe_set_timing(plan, 2) the device clock
  * records its span (moe_timings slots 7 and 8). */
 int moe_scale_gated(moe_plan *plan, const float *topk_w, const void *const *recv,
@@ -210,7 +210,8 @@ int moe_scale_gated(moe_plan *plan, const float *topk_w, const void *const *recv
  * of the combine's bytes whose copies had landed when the producer finished its last
  * output tile, *tail_us how long after that tile the last copy landed (negative if
  * before), *copy_bytes the bytes copied. Synchronises the device. MOE_ERR_ARG if no
- * such combine was recorded. Any output pointer may be NULL. */
+ * such combine was recorded; MOE_ERR_UNSUPPORTED if host memory for copies of the
+ * segment records and stamps cannot be had. Any output pointer may be NULL. */
 int moe_combine_overlap(moe_plan *plan, double *landed_frac, double *tail_us,
                         double *copy_bytes);
 

@@ -153,13 +153,22 @@ def test_gated_scale_equals_scale_after(wl, mode):
     gated.close()
 
 
-def test_gated_scale_once_per_combine():
+def test_gated_scale_once_per_combine_on_its_stream():
     wl = get_workload("tiny")
     inp = P.inputs_for(wl)
     layer = P.run_gpu(wl, inp, mode="fused", scale_mode="gated")
     assert layer.status() == (0, 0)
     with pytest.raises(capi.MoeError, match="MOE_ERR_ARG"):
         layer.scale_gated()  # no combine since the last one
+    sp, other = torch.cuda.Stream(), torch.cuda.Stream()
+    layer.route(inp.logits, inp.forced_ids, stream=sp)
+    layer.plan_build(inp.x, stream=sp)
+    layer.expert_combine(inp.w_gate, inp.w_up, inp.w_down, sp)
+    with pytest.raises(capi.MoeError, match="MOE_ERR_ARG"):
+        layer.scale_gated(stream=other)  # not ordered after the combine's zeroing
+    layer.scale_gated(stream=sp)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
     layer.close()
 
 

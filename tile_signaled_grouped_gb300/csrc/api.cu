@@ -46,6 +46,7 @@ struct moe_plan {
   bool timing;        // CUDA events around each kernel
   bool spans;         // device-clock records (span ring, chunk landing stamps)
   bool gated_armed;   // a combine was enqueued since the last moe_scale_gated
+  cudaStream_t combine_stream;  // the producer stream of the last combine
   bool gate_marked;   // the last routing call was moe_gate: its token bitmaps are in the plan
   const int32_t* gate_ids;  // the ids that moe_gate wrote
 };
@@ -517,6 +518,7 @@ int moe_expert_combine(moe_plan* p, const void* const* w_gate, const void* const
   const size_t z1 = p->offsets[PA_GROUP_SIG] + p->counts[PA_GROUP_SIG] * 4;
   CUDA_TRY(cudaMemsetAsync(p->plan_ws + z0, 0, z1 - z0, sp));
   p->gated_armed = true;
+  p->combine_stream = sp;
   if (fused) {
     tstart(p, kTProducer, sp);
     CUDA_TRY(launch_producer_pair(pa, pgrid, true, sp));
@@ -566,7 +568,10 @@ int moe_scale(moe_plan* p, const float* topk_w, const void* const* recv, void* c
 
 int moe_scale_gated(moe_plan* p, const float* topk_w, const void* const* recv, void* const* out,
                     moe_stream_t stream) {
-  if (p == nullptr || !aligned16(topk_w) || recv == nullptr || out == nullptr || !p->gated_armed)
+  // Only the combine's producer stream orders the kernel after the zeroing of the
+  // flags, signals and counters it waits on.
+  if (p == nullptr || !aligned16(topk_w) || recv == nullptr || out == nullptr || !p->gated_armed ||
+      reinterpret_cast<cudaStream_t>(stream) != p->combine_stream)
     return MOE_ERR_ARG;
   const Dims& d = p->d;
   ScaleArgs a;
@@ -600,10 +605,10 @@ int moe_combine_overlap(moe_plan* p, double* landed_frac, double* tail_us, doubl
   if (nseg > 0 && nch > 0) {
     int32_t* recs = new (std::nothrow) int32_t[(size_t)nseg * kSegRec];
     unsigned long long* st = new (std::nothrow) unsigned long long[nch];
-    if (recs == nullptr || st == nullptr) {
+    if (recs == nullptr || st == nullptr) {  // host memory for the copies of the records
       delete[] recs;
       delete[] st;
-      return MOE_ERR_ARG;
+      return MOE_ERR_UNSUPPORTED;
     }
     cudaError_t e = cudaMemcpy(recs, p->plan_ws + p->offsets[PA_SEG_REC],
                                (size_t)nseg * kSegRec * 4, cudaMemcpyDeviceToHost);
