@@ -365,6 +365,28 @@ def gpu_arm(args, rank, world, local_rank):
     return result
 
 
+class L2Flush:
+    """Evicts the L2 (129 MB) before a timed kernel: a 512 MB write, then a read of the
+    same 512 MB. The write alone would leave up to the L2's size in dirty lines, whose
+    write-back then lands inside the next timed kernel and counts against it (the gate
+    on A100-like measured 15.6 us after a write and 13.0 us after a write and a read);
+    the read replaces them with clean lines of a buffer no timed kernel touches."""
+
+    def __init__(self, nbytes=512 << 20):
+        import torch
+
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.words = self.buf.view(torch.int32)
+        self.out = torch.empty((), dtype=torch.int64, device="cuda")
+
+    def __call__(self, stream=None):
+        import torch
+
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            self.buf.zero_()
+            torch.sum(self.words, dim=0, dtype=torch.int64, out=self.out)
+
+
 def other_workloads(args, skip):
     """The other workload shapes at full size, each with the bench's default schedule
     (fused producer and copy, two batches in flight): whole-step time from CUDA events
@@ -433,27 +455,28 @@ def other_workloads(args, skip):
     return out
 
 
-def measure_gate(lay, x, wl, stream, iters, warmup, hbm):
-    """The gate kernel (router scores + softmax + top-k in one launch) on the tokens x
-    with the workload's seeded router, L2 flushed before each launch; CUDA events of
-    the library around each launch (launch latency included), median."""
+def measure_gate(lay, x, wl, stream, iters, warmup, hbm, splits=0):
+    """The gate (router scores + softmax + top-k in one launch) on the tokens x with the
+    workload's seeded router, L2 flushed before each launch (L2Flush); CUDA events of
+    the library around each launch (launch latency included) and the kernel's
+    device-clock span, medians. splits 0: the kernel moe_gate picks (for E <= 16 the
+    one that streams the token rows into registers); 1-8: the tcgen05 kernel."""
     import torch
 
     from tile_signaled_grouped_gb300.workloads import router_weights
 
     W, T, D, k = wl.W, wl.T, wl.d_model, wl.topk
     wr = router_weights(wl, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     lay.set_timing(False)
     for _ in range(warmup):
-        lay.gate(x, wr, stream=stream)
+        lay.gate(x, wr, stream=stream, splits=splits)
     torch.cuda.synchronize()
     g, gs = [], []
     for _ in range(iters):
-        with torch.cuda.stream(stream):
-            flush.zero_()
+        flush(stream)
         lay.set_timing(True)
-        lay.gate(x, wr, stream=stream)
+        lay.gate(x, wr, stream=stream, splits=splits)
         t = lay.timings()
         g.append(t[0])
         gs.append(t[9])
@@ -465,11 +488,13 @@ def measure_gate(lay, x, wl, stream, iters, warmup, hbm):
     span = statistics.median(gs)
     nbytes = 2.0 * D * W * T + 2.0 * D * wl.E + 8.0 * W * T * k
     flops = 2.0 * W * T * D * wl.E
-    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+    kernel = "gate_rows_kernel" if splits == 0 and wl.E <= 16 else "gate_kernel"
+    return {"kernel": kernel, "splits": splits,
+            "ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
             "tflops": flops / (ms * 1e-3) / 1e12,
             "timing": "CUDA events around the launch (launch latency included), "
-                      "L2 flushed before each, median of %d" % iters,
+                      "L2 flushed (512 MB write, then read) before each, median of %d" % iters,
             "span_ms": span, "span_gbs": nbytes / (span * 1e-3) / 1e9,
             "span_frac_hbm": nbytes / (span * 1e-3) / 1e9 / hbm,
             "span_timing": "device clock, first CTA start to last CTA end, median"}
@@ -504,6 +529,10 @@ def gate_arm(args):
         clk.mark_start()
         g = measure_gate(lay, inp.x, wl, sp, args.steps, args.warmup, hbm)
         clk.mark_end()
+    # The tcgen05 kernel on the same tokens, for comparison, where the automatic
+    # choice is the other kernel.
+    other = (measure_gate(lay, inp.x, wl, sp, args.steps, args.warmup, hbm, splits=1)
+             if wl.E <= 16 else None)
     lay.close()
     ntok = wl.W * wl.T
     return {
@@ -511,16 +540,19 @@ def gate_arm(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": g["ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded: x~N(0,1), router~N(0,1/D))",
-        "config": {"workload": wl.name, "kernel": "gate_kernel", "W": wl.W,
+        "config": {"workload": wl.name, "kernel": g["kernel"], "W": wl.W,
                    "experts": wl.E, "topk": wl.topk, "tokens_per_rank": wl.T,
-                   "d_model": wl.d_model, "l2": "flushed before each launch"},
-        "roofline": {"kernel": "gate_kernel", "bound": "hbm", "achieved": g["gbs"],
+                   "d_model": wl.d_model,
+                   "l2": "flushed before each launch (512 MB write, then read)"},
+        "roofline": {"kernel": g["kernel"], "bound": "hbm", "achieved": g["gbs"],
                      "peak": hbm, "unit": "GB/s", "frac": g["frac_hbm"], "traffic": None,
                      "span_ms": g["span_ms"], "span_achieved": g["span_gbs"],
                      "span_frac": g["span_frac_hbm"], "span_timing": g["span_timing"],
                      "peak_source": f"{src} HBM copy", "bytes_per_launch": g["bytes"],
                      "launch_ms": g["ms"], "launch_ms_source": g["timing"]},
         "tflops": g["tflops"],
+        "tcgen05_gate_split1": None if other is None else {
+            k: other[k] for k in ("ms", "span_ms", "span_frac_hbm", "frac_hbm")},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
@@ -543,7 +575,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         for i, name in enumerate(["route", "plan", "producer", "consumer", "scale", "gather"]):
             acc.setdefault(name, []).append(t[i])
     over = {n: statistics.median(v) for n, v in acc.items()}
-    # Serial mode, each stage from a cold L2 (a 512 MB write before it): the producer on
+    # Serial mode, each stage from a cold L2 (L2Flush before it): the producer on
     # all SMs, then the consumer on all SMs with every flag set (it follows the producer
     # on one stream, so nothing flushes between the two), the routing, the plan with
     # its gather, and the scale.
@@ -551,11 +583,10 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     from tile_signaled_grouped_gb300.runtime import ExpertCombine
     lay2 = ExpertCombine(W, wl.L, k, T, D, wl.d_ff, wl.tb_M, wl.mgb, 0,
                          producer_pairs=args.producer_pairs)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
 
     def cold():
-        with torch.cuda.stream(sp):
-            flush.zero_()
+        flush(sp)
 
     lay2.set_timing(True)
     for _ in range(iters):
@@ -630,9 +661,9 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     torch.cuda.synchronize()
     graph_ms = ev0.elapsed_time(ev1) / (iters * 4)
     del graph
-    # The gate kernel (router scores + softmax + top-k in one launch) on this shape's
-    # tokens with seeded router weights, L2 flushed before each launch. It is not
-    # part of the step (the workload's routing comes from its gate logits).
+    # The gate (router scores + softmax + top-k in one launch) on this shape's tokens
+    # with seeded router weights, L2 flushed before each launch. It is not part of the
+    # step (the workload's routing comes from its gate logits).
     gate = measure_gate(lay2, inp.x, wl, sp, iters, 3, hbm) if wl.E <= 256 else {}
     rank_rows = layer.field(capi.MOE_PLAN_RANK_ROWS).cpu().tolist()
     recv_rows = layer.field(capi.MOE_PLAN_RECV_ROWS).cpu().tolist()
@@ -662,7 +693,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         "gather_gbs": gather_bytes / (ser["gather"] * 1e-3) / 1e9,
         "gather_frac": gather_bytes / (ser["gather"] * 1e-3) / 1e9 / hbm,
         "hbm_stage_timing": ("serial schedule, CUDA events around each kernel, L2 flushed "
-                             "(512 MB write) before the routing, the plan build (the gather "
+                             "(512 MB write, then read) before the routing, the plan build (the gather "
                              "is its last kernel), the producer and the scale; the consumer "
                              "follows the producer on one stream with no flush between them"),
         "scale_in_step_gbs": (scale_bytes / (over["scale"] * 1e-3) / 1e9

@@ -131,13 +131,18 @@ int moe_route(moe_plan *plan, const float *logits, const int32_t *forced_ids,
  *              16-byte aligned.
  *  forced_ids, topk_ids, topk_w: as moe_route.
  *  logits:     NULL, or out [W][T][E] fp32: the scores the routing used.
- *  splits:     0 picks the K split; 1, 2, 4 or 8 forces it (that many CTAs of one
- *              cluster share a 128-token tile, each summing a range of D; their
- *              partial sums are added in a fixed order, so a given split gives
- *              the same bits on every call).
- * Each tile holds as many tokens (a multiple of 8, at most 128) as fill one wave of
- * CTAs. The routing tail also sets the plan's token bitmaps (prescribed ids out of
- * range or repeated set MOE_DEV_ROUTING), for a following moe_plan_build(plan, NULL, ...).
+ *  splits:     0 picks the kernel: for E <= 16 one that streams the token rows
+ *              from HBM into registers and takes the scores with mma.sync (the
+ *              contraction is 8 or 16 columns wide and the launch a one-shot read
+ *              of x); above, the tcgen05 kernel with the K split it picks. 1, 2, 4
+ *              or 8 force the tcgen05 kernel with that split (that many CTAs of one
+ *              cluster share a 128-token tile, each summing a range of D).
+ * Both kernels add each score's partial sums in a fixed order, so a given choice
+ * gives the same bits on every call; the two kernels' scores differ by rounding
+ * only. A tcgen05 tile holds as many tokens (a multiple of 8, at most 128) as fill
+ * one wave of CTAs, and so does a CTA of the other kernel (at most 128 tokens).
+ * The routing tail also sets the plan's token bitmaps (prescribed ids out of range
+ * or repeated set MOE_DEV_ROUTING), for a following moe_plan_build(plan, NULL, ...).
  * E <= 256; larger E, or a split the GPU cannot hold, gives MOE_ERR_UNSUPPORTED.
  * The caller owns every buffer. Timed in slot [0] of moe_timings, its device-clock
  * span in slot [9]. */

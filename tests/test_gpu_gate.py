@@ -1,5 +1,6 @@
-"""Parity of the gate kernel (router scores on the tensor cores, fused with the
-softmax and the top k) against the float64 oracle, through the C ABI.
+"""Parity of the two gate kernels (router scores fused with the softmax and the top
+k: on tcgen05, or for E <= 16 with the token rows streamed into registers and the
+scores on mma.sync) against the float64 oracle, through the C ABI.
 
 Tolerance (derived from the arithmetic). Each score is a sum of D products of
 bf16 values; every product is exact in fp32, and the kernel adds them (and the
@@ -131,7 +132,33 @@ GATE_SHAPES = [
 @pytest.mark.parametrize("splits", [0, 1, 2, 4, 8])
 @pytest.mark.parametrize("wl", GATE_SHAPES, ids=lambda w: w.name)
 def test_gate_parity(wl, splits):
+    """splits 0 is the automatic choice: the kernel that streams the token rows into
+    registers for E <= 16 (E8_T150, k_equals_E), the tcgen05 kernel above; 1-8 are the
+    tcgen05 kernel's K splits."""
     ids_g, w_g, lg_g, xs, wr, _ = run_gate(wl, splits)
+    check_gate(wl, xs, wr, ids_g, w_g, lg_g)
+
+
+# Shapes for the kernel that streams the token rows into registers (E <= 16, taken
+# with splits 0): one and two n-tiles of 8 experts with padded experts, a single
+# expert, every expert chosen, one token per rank, tokens per CTA that are not a
+# multiple of the 16-token group, and more CTAs than one wave.
+ROWS_SHAPES = [
+    Workload("rows_E1", W=1, L=1, topk=1, T=37, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    Workload("rows_E9_T2500", W=3, L=3, topk=3, T=2500, d_model=384, d_ff=128, tb_M=64,
+             routing="gate"),
+    Workload("rows_E12_T333", W=4, L=3, topk=3, T=333, d_model=640, d_ff=128, tb_M=64,
+             routing="gate"),
+    Workload("rows_E16_k16_T1", W=8, L=2, topk=16, T=1, d_model=256, d_ff=128, tb_M=64,
+             routing="gate"),
+    Workload("rows_E8_waves", W=1, L=8, topk=2, T=20000, d_model=128, d_ff=128, tb_M=64,
+             routing="gate"),
+]
+
+
+@pytest.mark.parametrize("wl", ROWS_SHAPES, ids=lambda w: w.name)
+def test_rows_gate_parity(wl):
+    ids_g, w_g, lg_g, xs, wr, _ = run_gate(wl)
     check_gate(wl, xs, wr, ids_g, w_g, lg_g)
 
 
@@ -151,10 +178,11 @@ def test_gate_prescribed_ids_keep_the_scores_probabilities():
     check_gate(wl, xs, wr, ids_g, w_g, None, forced)
 
 
-def test_gate_is_deterministic_for_a_split():
-    wl = GATE_SHAPES[4]
-    a = run_gate(wl, splits=4)
-    b = run_gate(wl, splits=4)
+@pytest.mark.parametrize("wl,splits", [(GATE_SHAPES[4], 4), (ROWS_SHAPES[2], 0)],
+                         ids=["tcgen05_split4", "rows"])
+def test_gate_is_deterministic_for_a_split(wl, splits):
+    a = run_gate(wl, splits=splits)
+    b = run_gate(wl, splits=splits)
     for x, y in zip(a[:3], b[:3]):
         assert np.array_equal(x, y)
 

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_tsg.so")
 SOURCES = ["api.cu", "plan.cu", "ffn.cu", "ffn_pair.cu", "consumer.cu", "route_scale.cu", "gate.cu",
-           "plan_noalloc.cu"]
+           "plan_noalloc.cu", "gate_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -298,7 +298,7 @@ int moe_plan_create(const moe_cfg* cfg, void* plan_ws, size_t plan_ws_bytes, voi
   if (preload_producer() != cudaSuccess || preload_producer_pair() != cudaSuccess ||
       preload_consumer() != cudaSuccess ||
       preload_plan() != cudaSuccess || preload_route_scale() != cudaSuccess ||
-      preload_gate() != cudaSuccess)
+      preload_gate() != cudaSuccess || preload_gate_rows() != cudaSuccess)
     return MOE_ERR_CUDA;
 
   void* fn = nullptr;
@@ -373,46 +373,64 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
     return MOE_ERR_ARG;
   if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8) return MOE_ERR_ARG;
   const Dims& d = p->d;
+  for (int r = 0; r < d.W; ++r)
+    if (!aligned16(x[r])) return MOE_ERR_ARG;
   const int lg = splits == 8 ? 3 : splits == 4 ? 2 : splits == 2 ? 1 : 0;
   if (p->gate_npad == 0 || (splits != 0 && p->gate_clusters[lg] == 0)) return MOE_ERR_UNSUPPORTED;
+  // splits == 0 with E <= 16 (and a router that fits in shared memory): the kernel
+  // that streams the token rows into registers; otherwise the tcgen05 kernel.
+  const bool rows_kernel = splits == 0 && gate_rows_fits(d.E, d.D);
   GateArgs ga{};
-  ga.npad = p->gate_npad;
-  ga.forced = forced;
-  ga.ids = ids;
-  ga.w = w;
-  ga.logits = logits;
-  ga.p = dev_plan(p);
-  if (splits == 0) {
-    // The largest split whose clusters all run at once (one wave: a second wave
-    // costs a whole tile's time) and that leaves every CTA at least four K blocks.
-    const int tiles = d.W * ((d.T + kTileM - 1) / kTileM);
-    const int nk = d.D / kBlockK;
-    splits = 1;
-    for (int i = 1; i < 4; ++i)
-      if (tiles <= p->gate_clusters[i] && nk >= (4 << i)) splits = 1 << i;
+  GateRowsArgs ra{};
+  if (rows_kernel) {
+    for (int r = 0; r < d.W; ++r) ra.x[r] = static_cast<const __nv_bfloat16*>(x[r]);
+    ra.router = static_cast<const __nv_bfloat16*>(w_router);
+    ra.forced = forced;
+    ra.ids = ids;
+    ra.w = w;
+    ra.logits = logits;
+    ra.p = dev_plan(p);
+    gate_rows_shape(d.W, d.T, d.E, d.D, p->num_sms, &ra.rows, &ra.kslices);
+  } else {
+    ga.npad = p->gate_npad;
+    ga.forced = forced;
+    ga.ids = ids;
+    ga.w = w;
+    ga.logits = logits;
+    ga.p = dev_plan(p);
+    if (splits == 0) {
+      // The largest split whose clusters all run at once (one wave: a second wave
+      // costs a whole tile's time) and that leaves every CTA at least four K blocks.
+      const int tiles = d.W * ((d.T + kTileM - 1) / kTileM);
+      const int nk = d.D / kBlockK;
+      splits = 1;
+      for (int i = 1; i < 4; ++i)
+        if (tiles <= p->gate_clusters[i] && nk >= (4 << i)) splits = 1 << i;
+    }
+    ga.splits = splits;
+    // Tokens per tile: as few (a multiple of 8, at most 128) as fill one wave of
+    // clusters, so that every SM streams its share of the token rows.
+    {
+      const int lgs = splits == 8 ? 3 : splits == 4 ? 2 : splits == 2 ? 1 : 0;
+      const int per_rank = std::max(1, p->gate_clusters[lgs] / d.W);
+      const int want = (d.T + per_rank - 1) / per_rank;
+      ga.rows = std::min(kTileM, std::max(8, (want + 7) / 8 * 8));
+    }
+    for (int r = 0; r < d.W; ++r)
+      if (!make_map(p, &ga.tm_x[r], x[r], d.T, d.D, (uint32_t)ga.rows)) return MOE_ERR_ARG;
+    if (!make_map(p, &ga.tm_r, w_router, d.E, d.D, (uint32_t)ga.npad)) return MOE_ERR_ARG;
   }
-  ga.splits = splits;
-  // Tokens per tile: as few (a multiple of 8, at most 128) as fill one wave of
-  // clusters, so that every SM streams its share of the token rows.
-  {
-    const int lg = splits == 8 ? 3 : splits == 4 ? 2 : splits == 2 ? 1 : 0;
-    const int per_rank = std::max(1, p->gate_clusters[lg] / d.W);
-    const int want = (d.T + per_rank - 1) / per_rank;
-    ga.rows = std::min(kTileM, std::max(8, (want + 7) / 8 * 8));
-  }
-  for (int r = 0; r < d.W; ++r)
-    if (!aligned16(x[r]) || !make_map(p, &ga.tm_x[r], x[r], d.T, d.D, (uint32_t)ga.rows))
-      return MOE_ERR_ARG;
-  if (!make_map(p, &ga.tm_r, w_router, d.E, d.D, (uint32_t)ga.npad)) return MOE_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The routing tail sets the plan's token bitmaps: they start at zero.
   CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_BITMAP], 0, p->counts[PA_BITMAP] * 4, s));
   if (p->spans) {
-    ga.p.span = span_record(p, p->nspan);
-    CUDA_TRY(cudaMemsetAsync(ga.p.span + kSpanGateStart, 0, 2 * sizeof(unsigned long long), s));
+    unsigned long long* span = span_record(p, p->nspan);
+    ga.p.span = span;
+    ra.p.span = span;
+    CUDA_TRY(cudaMemsetAsync(span + kSpanGateStart, 0, 2 * sizeof(unsigned long long), s));
   }
   tstart(p, kTRoute, s);
-  CUDA_TRY(launch_gate(ga, s));
+  CUDA_TRY(rows_kernel ? launch_gate_rows(ra, s) : launch_gate(ga, s));
   tstop(p, kTRoute, s);
   p->gate_marked = true;
   p->gate_ids = ids;

@@ -83,35 +83,6 @@ struct GSmem {
   int abort;
 };
 
-// The plan's token bitmap (TileMoE notes section 4.2: rows are grouped by expert and
-// source rank, in source-token order): one bit per (expert, source rank, token), set
-// for every routing slot of token t of rank s, so that the plan build after a gate
-// skips its bitmap kernel (the group counts stay in the plan's count kernel, which,
-// unlike this kernel, fits beside a running producer CTA). G = 1: this thread routed the token;
-// G = 32: lane j < k wrote slot j. The gate's own top k is k distinct ids in range;
-// prescribed ids are checked like the plan build checks them (out of range or
-// repeated within the token: MOE_DEV_ROUTING, the slot skipped).
-template <int G>
-__device__ __forceinline__ void mark_token(const GateArgs& a, const Dims& d, size_t tok, int s,
-                                           int t, int lig, uint32_t* status) {
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(a.p.a[PA_BITMAP]);
-  const int32_t* row = a.ids + tok * d.k;
-  const bool check = a.forced != nullptr;
-  if (G > 1 && check) __syncwarp();  // the ids the other lanes wrote
-  for (int j = G > 1 ? lig : 0; j < d.k; j += G) {
-    const int e = row[j];
-    if (check) {
-      bool ok = e >= 0 && e < d.E;
-      for (int q = 0; q < j && ok; ++q) ok = row[q] != e;
-      if (!ok) {
-        report_error(status, MOE_DEV_ROUTING, (uint32_t)tok);
-        continue;
-      }
-    }
-    atomicOr(&bitmap[((size_t)e * d.W + s) * d.TW + (t >> 5)], 1u << (t & 31));
-  }
-}
-
 template <int G, int PER>
 __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_constant__ GateArgs a) {
   extern __shared__ uint8_t gate_smem_raw[];
@@ -293,9 +264,12 @@ __global__ void __launch_bounds__(kGateThreads, 1) gate_kernel(const __grid_cons
         v[i] = e < d.E ? row[e] : -INFINITY;
         if (e < d.E && a.logits != nullptr) a.logits[tok * d.E + e] = v[i];
       }
+      const TokenMark mk{reinterpret_cast<uint32_t*>(a.p.a[PA_BITMAP]), (size_t)d.W * d.TW,
+                         (size_t)s * d.TW + (t >> 5), 1u << (t & 31)};
       route_group<G, PER>(v, d.E, d.k, a.forced != nullptr ? a.forced + tok * d.k : nullptr,
-                          a.ids + tok * d.k, a.w + tok * d.k, lig);
-      mark_token<G>(a, d, tok, s, t, lig, status);
+                          a.ids + tok * d.k, a.w + tok * d.k, lig,
+                          a.forced != nullptr ? nullptr : &mk);
+      if (a.forced != nullptr) mark_token<G>(a.p, a.ids, a.forced, tok, s, t, lig, status);
     }
   }
 

@@ -150,6 +150,26 @@ cudaError_t preload_gate();
 int gate_clusters(int E, int splits);
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
 
+// The gate for E <= 16 with the token rows streamed into registers (gate_rows.cu).
+struct GateRowsArgs {
+  const __nv_bfloat16* x[MOE_MAX_RANKS];  // rank s's tokens [T][D]
+  const __nv_bfloat16* router;            // [E][D]
+  const int32_t* forced;                  // [W][T][k] or null
+  int32_t* ids;                           // [W][T][k]
+  float* w;                               // [W][T][k]
+  float* logits;                          // [W][T][E] or null
+  DevPlan p;
+  int rows;     // tokens per CTA, at most 128 (CTA j of rank s: tokens [j*rows, ...))
+  int kslices;  // warps sharing a 16-token group, each a contiguous range of 64 columns
+};
+cudaError_t preload_gate_rows();
+// Whether the kernel takes E experts of D columns (E <= 16, its router and partial
+// sums in shared memory).
+bool gate_rows_fits(int E, int D);
+// Tokens per CTA and K slices for T tokens per rank on W ranks and num_sms SMs.
+void gate_rows_shape(int W, int T, int E, int D, int num_sms, int* rows, int* kslices);
+cudaError_t launch_gate_rows(const GateRowsArgs& a, cudaStream_t s);
+
 struct ProducerArgs {
   CUtensorMap tm_x[MOE_MAX_RANKS];
   CUtensorMap tm_h[MOE_MAX_RANKS];

@@ -1,11 +1,12 @@
-// Routing of one token by a warp or by one thread: softmax over its E gate scores
-// and the top k.
+// Routing of one token by a warp, by the 8 lanes of an octet or by one thread: softmax
+// over its E gate scores and the top k.
 //
 // TileMoE notes (zhongzhuzhou.org), section 2.1 and 2.2 step 1: the router turns a
 // token's scores into a probability distribution over the E experts and keeps the
 // k most probable ones; the gate weights are those probabilities (not renormalised
 // over the k). Used by the routing kernel (a warp per token, scores read from
-// memory) and by the gate kernel (scores summed from its K-split partials).
+// memory) and by the two gate kernels (scores summed from their K-split partials),
+// which also mark each routed token in the plan's bitmap (TokenMark, mark_token).
 #pragma once
 
 #include "moe_common.cuh"
@@ -63,13 +64,24 @@ __device__ __forceinline__ void route_sort(float (&v)[PER], int (&e)[PER]) {
   }
 }
 
+// Where a routed token's bits go in the plan's token bitmap (see mark_token): the
+// word of expert e is bitmap[e * per_expert + word], the token's bit in it `bit`.
+struct TokenMark {
+  uint32_t* bitmap;
+  size_t per_expert;
+  size_t word;
+  uint32_t bit;
+};
+
 // One token, routed by G = 32 lanes (a whole warp, converged) or by G = 1 thread.
 // Lane lig of the group holds the scores of experts lig, lig + G, ... (PER of them;
 // -inf past E). Writes ids_row[0..k) and w_row[0..k) (from lig == 0). The decision
 // compares scores, larger first, equal scores to the lower expert id: the order of
 // the probabilities without their rounding ties. With forced_row, the ids are
 // those and the weights the probabilities at them (0 for an id out of range, which
-// the plan build reports).
+// the plan build reports). With `mark` (a gate's own top k, not prescribed ids), the
+// thread that writes slot j also sets the token's bit of that expert in the plan's
+// token bitmap, from the id it holds (no read back of the row it wrote).
 //
 // Cost. Every step is branch-free: padded candidates hold -inf, so exp adds an
 // exact 0 for them and they never win. A warp's reductions are redux.sync over all
@@ -83,7 +95,8 @@ __device__ __forceinline__ void route_sort(float (&v)[PER], int (&e)[PER]) {
 template <int G, int PER>
 __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int k,
                                             const int32_t* forced_row, int32_t* ids_row,
-                                            float* w_row, int lig) {
+                                            float* w_row, int lig,
+                                            const TokenMark* mark = nullptr) {
   static_assert(G == 1 || G == 32, "a thread or a whole warp per token");
   static_assert(PER <= 32, "candidates per lane");
   constexpr uint32_t kAll = 0xFFFFFFFFu;
@@ -148,11 +161,13 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
       } else {
         ids_row[j] = (int32_t)emin;
         w_row[j] = expf(key_float(kmax) - mx) * inv;
+        if (mark != nullptr) atomicOr(mark->bitmap + emin * mark->per_expert + mark->word, mark->bit);
       }
     }
     if (G > 1 && lig < k) {
       ids_row[lig] = (int32_t)my_id;
       w_row[lig] = expf(key_float(my_key) - mx) * inv;
+      if (mark != nullptr) atomicOr(mark->bitmap + my_id * mark->per_expert + mark->word, mark->bit);
     }
   } else {
     uint32_t taken = 0;  // bit i: this lane's candidate i already chosen
@@ -182,12 +197,103 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
       } else {
         ids_row[j] = (int32_t)emin;
         w_row[j] = expf(key_float(kmax) - mx) * inv;
+        if (mark != nullptr) atomicOr(mark->bitmap + emin * mark->per_expert + mark->word, mark->bit);
       }
     }
     if (G > 1 && lig < k) {
       ids_row[lig] = (int32_t)my_id;
       w_row[lig] = expf(key_float(my_key) - mx) * inv;
+      if (mark != nullptr) atomicOr(mark->bitmap + my_id * mark->per_expert + mark->word, mark->bit);
     }
+  }
+}
+
+// One token routed by the 8 lanes of an octet (lanes 8o .. 8o + 7 of a converged
+// warp; the warp's four octets route four tokens at once). Lane li holds the scores of
+// experts li + 8i (PER of them, -inf past E), k <= E. The decision and the weights are
+// route_group's: larger score first, equal scores to the lower id; weight = the
+// softmax probability at the chosen id. The maximum, the sum of the exponentials and
+// each round's winner are butterflies over the octet (xor 4, 2, 1); fp32 addition and
+// the (score, id) order are commutative, so every lane of the octet ends with the same
+// values. Where a thread per token runs a chain of some hundred dependent steps, the
+// octet runs a dozen shuffles. Lane 0 of an active octet writes slot j (and, with
+// `mark`, the token's bit of that expert).
+template <int PER>
+__device__ __forceinline__ void route_octet(const float (&vin)[PER], int k, int32_t* ids_row,
+                                            float* w_row, int li, bool active,
+                                            const TokenMark* mark) {
+  constexpr uint32_t kAll = 0xFFFFFFFFu;
+  float mx = vin[0];
+#pragma unroll
+  for (int i = 1; i < PER; ++i) mx = fmaxf(mx, vin[i]);
+#pragma unroll
+  for (int o = 4; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) sum += expf(vin[i] - mx);
+#pragma unroll
+  for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(kAll, sum, o);
+  const float inv = 1.0f / sum;
+  uint32_t key[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) key[i] = float_key(vin[i]);
+  uint32_t taken = 0;  // bit i: this lane's candidate i already chosen
+  for (int j = 0; j < k; ++j) {
+    // This lane's best candidate not yet taken (key 0: none; every score has a key > 0).
+    uint32_t bk = 0, be = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const uint32_t e = (uint32_t)(li + 8 * i);
+      const bool better = !((taken >> i) & 1u) & ((key[i] > bk) | ((key[i] == bk) & (e < be)));
+      bk = better ? key[i] : bk;
+      be = better ? e : be;
+    }
+#pragma unroll
+    for (int o = 4; o; o >>= 1) {
+      const uint32_t ok = __shfl_xor_sync(kAll, bk, o), oe = __shfl_xor_sync(kAll, be, o);
+      const bool take = (ok > bk) | ((ok == bk) & (oe < be));
+      bk = take ? ok : bk;
+      be = take ? oe : be;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) taken |= ((uint32_t)(li + 8 * i) == be) ? 1u << i : 0u;
+    if (active && li == 0) {
+      ids_row[j] = (int32_t)be;
+      w_row[j] = expf(key_float(bk) - mx) * inv;
+      if (mark != nullptr) atomicOr(mark->bitmap + be * mark->per_expert + mark->word, mark->bit);
+    }
+  }
+}
+
+// The plan's token bitmap (TileMoE notes section 4.2: rows are grouped by expert and
+// source rank, in source-token order): one bit per (expert, source rank, token), set
+// for every routing slot of token t of rank s, so that the plan build after a gate
+// skips its bitmap kernel (the group counts stay in the plan's count kernel, which,
+// unlike the gate kernels, fits beside a running producer CTA). A gate's own top k
+// (k distinct ids in range) is marked inside route_group (TokenMark); this function
+// marks prescribed ids, checked like the plan build checks them (out of range or
+// repeated within the token: MOE_DEV_ROUTING, the slot skipped). G = 1: this thread
+// routed the token; G = 32: lane j < k wrote slot j.
+template <int G>
+__device__ __forceinline__ void mark_token(const DevPlan& p, const int32_t* ids,
+                                           const int32_t* forced, size_t tok, int s, int t,
+                                           int lig, uint32_t* status) {
+  const Dims& d = p.d;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(p.a[PA_BITMAP]);
+  const int32_t* row = ids + tok * d.k;
+  const bool check = forced != nullptr;
+  if (G > 1 && check) __syncwarp();  // the ids the other lanes wrote
+  for (int j = G > 1 ? lig : 0; j < d.k; j += G) {
+    const int e = row[j];
+    if (check) {
+      bool ok = e >= 0 && e < d.E;
+      for (int q = 0; q < j && ok; ++q) ok = row[q] != e;
+      if (!ok) {
+        report_error(status, MOE_DEV_ROUTING, (uint32_t)tok);
+        continue;
+      }
+    }
+    atomicOr(&bitmap[((size_t)e * d.W + s) * d.TW + (t >> 5)], 1u << (t & 31));
   }
 }
 
