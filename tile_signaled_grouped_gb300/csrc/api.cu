@@ -121,7 +121,7 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_GROUP_NSEG] = W * W;
   n[PA_RANK_TILES] = 2 * W * NMM;
   n[PA_TILE_ROW] = n[PA_TILE_EXPERT] = W * NMM;
-  n[PA_UNIT_BEGIN] = W * (NMM / kTileGroup + 2) + 1;
+  n[PA_UNIT_BEGIN] = 2 * W * (size_t)unit_cap(d) + 1;
   n[PA_SEG_ORDER] = W * NBM;
   n[PA_SEG_REC] = W * NBM * kSegRec;
   n[PA_GROUP_NCHUNK] = W * W;
@@ -135,6 +135,7 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   // remote rows (at most W * T * topk) cut into chunks of rpc rows.
   n[PA_CHUNK_REC] = W * (size_t)d.T * d.k / d.rpc + W * NBM + 1;
   n[PA_CHUNK_T] = 2 * n[PA_CHUNK_REC];
+  n[PA_UNIT_TMP] = 4 * W * (size_t)unit_cap(d);
   size_t pos = 0;
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;

@@ -20,7 +20,7 @@ constexpr int kBlockK = 64;      // K elements per pipeline stage (128 B of bf16
 constexpr int kN1 = 128;         // GEMM1 hidden columns per tile (gate and up each)
 constexpr int kStages = 4;       // shared-memory pipeline depth
 constexpr int kTaskRing = 4;     // task descriptors in flight inside one CTA
-constexpr int kTileGroup = 32;   // tiles per scheduling unit (weight reuse in L2)
+constexpr int kTileGroup = 32;   // tiles per scheduling unit at most (weight reuse in L2)
 constexpr int kProducerThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kConsumerThreads = 32;         // one warp: lane 0 drives the bulk copies
 constexpr int kChunkBytes = 20 * 1024;       // consumer copy chunk (one shared-memory slot)
@@ -59,6 +59,12 @@ struct Dims {
   int rpc;       // rows per consumer copy chunk
 };
 
+// Scheduling units of one rank and phase (remote or local tiles) at most. A unit
+// starts only at the start of an expert's run of tiles (at most L runs per phase) or
+// inside a run longer than kTileGroup (a new unit every kTileGroup tiles at most), so
+// a phase of n <= NMM tiles has at most L + n / kTileGroup + 1 units.
+__host__ __device__ inline int unit_cap(const Dims& d) { return d.L + d.NMM / kTileGroup + 1; }
+
 // Fields of the plan workspace, in placement order. The public moe_field enum
 // exposes a subset; the rest are internal.
 enum PlanArray {
@@ -82,6 +88,8 @@ enum PlanArray {
   PA_XPREV,  // [W][RM] what each X row held after the last gather: token, -1 zero, else unknown
   PA_CHUNK_T,  // [chunks] u64: device clock when each copy chunk had landed (timing on)
   PA_CHUNK_REC,  // [chunks] segment record (consumer order) of every copy chunk
+  PA_UNIT_TMP,   // [2][W][2][unit_cap] plan-internal: each unit's first tile in its rank's
+                 // phase, then its position in the global tile order
   PA_COUNT
 };
 

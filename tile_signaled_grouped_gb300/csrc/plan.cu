@@ -343,37 +343,25 @@ __global__ void plan_scatter_kernel(DevPlan p, const int32_t* __restrict__ ids) 
   }
 }
 
-// Position of item q of rank o when every rank's sequence is cut into chunks of
-// `g` and the chunks are taken round-robin over the ranks, chunk index first.
-__device__ __forceinline__ int rr_position(const int* len, int W, int o, int q, int g) {
-  const int c = q / g, w = q % g;
-  int pos = w;
-  for (int o2 = 0; o2 < W; ++o2) {
-    pos += min(c * g, len[o2]);
-    if (o2 < o) pos += min(g, max(0, len[o2] - c * g));
-  }
-  return pos;
-}
-__device__ __forceinline__ int rr_unit(const int* len, int W, int o, int q, int g) {
-  const int c = q / g;
-  int u = 0;
-  for (int o2 = 0; o2 < W; ++o2) {
-    u += min(c, (len[o2] + g - 1) / g);
-    if (o2 < o && len[o2] > c * g) ++u;
-  }
-  return u;
-}
-
-// Single CTA: the producer's tile order (remote tiles of every rank first, in
-// chunks of kTileGroup tiles round-robin over the ranks, each rank in its S order;
-// then the local tiles the same way), its scheduling units, and the consumer's
-// segment order (following the tile order).
+// Single CTA: the producer's tile order and its scheduling units, and the consumer's
+// segment order (following the tile order). Each rank's remote tiles, then its local
+// tiles (its S order), are cut into scheduling units of at most kTileGroup tiles
+// that keep each expert's run of tiles (S keeps an expert's remote tiles, and its
+// local tiles, contiguous) inside one unit wherever it fits: the runs are packed in
+// order, a new unit opened when the next run does not fit, and a run longer than
+// kTileGroup cut into near-equal parts of even length (CTA pairs stay together). A
+// unit's GEMM1 reads each weight tile of its experts once (its tasks are hidden-
+// column-major), so a run split over two units would read its expert's weights
+// twice. The units of the remote phase come first, round-robin over the ranks (unit
+// 0 of every rank, then unit 1, ...), then those of the local phase.
 __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
   const Dims d = p.d;
   const int tid = threadIdx.x, nt = blockDim.x;
   __shared__ int scratch[33];
   __shared__ int s_nt[MOE_MAX_RANKS], s_rt[MOE_MAX_RANKS], s_lt[MOE_MAX_RANKS];
   __shared__ int s_rem[MOE_MAX_RANKS], s_nb[MOE_MAX_RANKS], s_nseg[MOE_MAX_RANKS];
+  __shared__ int s_nu[MOE_MAX_RANKS][2], s_NU;
+  __shared__ int s_ecnt[2 * 1024];  // tiles of each (expert, phase); E <= 1024
   const int W = d.W, tb = d.tb;
   const int P = tb >= kTileM ? tb / kTileM : 1;
   int32_t* rank_tiles = p.a[PA_RANK_TILES];  // [W][NMM] rank-local row of each tile, S order
@@ -430,15 +418,74 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
   if (tid < W) s_lt[tid] = s_nt[tid] - s_rt[tid];
   __syncthreads();
 
-  int RT = 0, NM = 0, NUR = 0, NU = 0;
-  for (int o = 0; o < W; ++o) {
-    RT += s_rt[o];
-    NM += s_nt[o];
-    NUR += (s_rt[o] + kTileGroup - 1) / kTileGroup;
-    NU += (s_rt[o] + kTileGroup - 1) / kTileGroup + (s_lt[o] + kTileGroup - 1) / kTileGroup;
-  }
+  int NM = 0;
+  for (int o = 0; o < W; ++o) NM += s_nt[o];
 
-  // 2. Global tile order, units, and the tile of every band.
+  // 2. Scheduling units. Tiles of each (expert, phase), then one thread per (rank,
+  // phase) walks its expert runs and records where each unit starts.
+  const int cap = unit_cap(d);
+  int32_t* ustart = p.a[PA_UNIT_TMP];       // [W][2][cap] first tile of each unit in its phase
+  int32_t* ugpos = ustart + 2 * W * cap;    // [W][2][cap] its position in the tile order
+  for (int i = tid; i < 2 * d.E; i += nt) s_ecnt[i] = 0;
+  __syncthreads();
+  for (int o = 0; o < W; ++o) {
+    const int32_t* rt = rank_tiles + (size_t)o * d.NMM;
+    const int32_t* bexp = p.a[PA_BAND_EXPERT] + (size_t)o * d.NBM;
+    for (int q = tid; q < s_nt[o]; q += nt)
+      atomicAdd(&s_ecnt[2 * bexp[rt[q] / tb] + (q < s_rt[o] ? 0 : 1)], 1);
+  }
+  __syncthreads();
+  if (tid < 2 * W) {
+    const int o = tid >> 1, ph = tid & 1;
+    const int q0 = ph ? s_rt[o] : 0, q1 = ph ? s_nt[o] : s_rt[o];
+    const int32_t* rt = rank_tiles + (size_t)o * d.NMM;
+    const int32_t* bexp = p.a[PA_BAND_EXPERT] + (size_t)o * d.NBM;
+    int32_t* us = ustart + (size_t)(o * 2 + ph) * cap;
+    int nu = 0, open = -1;  // phase-local first tile of the open unit (-1: none)
+    for (int q = q0; q < q1;) {
+      const int len = s_ecnt[2 * bexp[rt[q] / tb] + ph];  // this expert's run (>= 1)
+      const int qq = q - q0;
+      if (len > kTileGroup) {
+        const int n = (len + kTileGroup - 1) / kTileGroup;
+        const int part = 2 * ((len + 2 * n - 1) / (2 * n));  // even, at most kTileGroup
+        for (int i = 0; i < n && i * part < len; ++i) us[nu++] = qq + i * part;
+        open = -1;
+      } else if (open < 0 || qq + len - open > kTileGroup) {
+        us[nu++] = qq;
+        open = qq;
+      }
+      q += len;
+    }
+    s_nu[o][ph] = nu;
+  }
+  __syncthreads();
+  // Positions: the remote units round-robin over the ranks, then the local ones.
+  if (tid == 0) {
+    int u = 0, pos = 0;
+    for (int ph = 0; ph < 2; ++ph) {
+      int maxnu = 0;
+      for (int o = 0; o < W; ++o) maxnu = max(maxnu, s_nu[o][ph]);
+      for (int j = 0; j < maxnu; ++j)
+        for (int o = 0; o < W; ++o) {
+          const int nuo = s_nu[o][ph];
+          if (j >= nuo) continue;
+          const int32_t* us = ustart + (size_t)(o * 2 + ph) * cap;
+          const int tiles = ph ? s_lt[o] : s_rt[o];
+          ugpos[(size_t)(o * 2 + ph) * cap + j] = pos;
+          p.a[PA_UNIT_BEGIN][u++] = pos;
+          pos += (j + 1 < nuo ? us[j + 1] : tiles) - us[j];
+        }
+    }
+    p.a[PA_UNIT_BEGIN][u] = NM;
+    p.a[PA_TOTALS][0] = NM;
+    p.a[PA_TOTALS][2] = u;
+    s_NU = u;
+  }
+  __syncthreads();
+  const int NU = s_NU;
+
+  // 2a. Global tile order and the tile of every band: a tile's unit is the last one
+  // starting at or before it in its phase.
   for (int o = 0; o < W; ++o) {
     const int32_t* rt = rank_tiles + (size_t)o * d.NMM;
     const int32_t* bexp = p.a[PA_BAND_EXPERT] + (size_t)o * d.NBM;
@@ -446,17 +493,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
     const int32_t* ralloc = p.a[PA_ROWS_ALLOC] + o * d.L;
     int32_t* btile = p.a[PA_BAND_TILE] + (size_t)o * d.NBM;
     for (int q = tid; q < s_nt[o]; q += nt) {
-      const bool remote = q < s_rt[o];
-      const int qq = remote ? q : q - s_rt[o];
-      const int* len = remote ? s_rt : s_lt;
-      const int pos = (remote ? 0 : RT) + rr_position(len, W, o, qq, kTileGroup);
+      const int ph = q < s_rt[o] ? 0 : 1;
+      const int qq = ph ? q - s_rt[o] : q;
+      const int32_t* us = ustart + (size_t)(o * 2 + ph) * cap;
+      int lo = 0, hi = s_nu[o][ph] - 1;  // us[0] == 0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (us[mid] <= qq) lo = mid; else hi = mid - 1;
+      }
+      const int pos = ugpos[(size_t)(o * 2 + ph) * cap + lo] + (qq - us[lo]);
       const int row = rt[q];
       const int b = row / tb;
       const int e = bexp[b];
       p.a[PA_TILE_ROW][pos] = (o << 24) | row;
       p.a[PA_TILE_EXPERT][pos] = e;
-      if (qq % kTileGroup == 0)
-        p.a[PA_UNIT_BEGIN][(remote ? 0 : NUR) + rr_unit(len, W, o, qq, kTileGroup)] = pos;
       if (tb >= kTileM) {
         if (row % tb == 0) btile[b] = pos;
       } else {
@@ -465,11 +515,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
         if ((b + 1) * tb < estart[li] + ralloc[li]) btile[b + 1] = pos;
       }
     }
-  }
-  if (tid == 0) {
-    p.a[PA_UNIT_BEGIN][NU] = NM;
-    p.a[PA_TOTALS][0] = NM;
-    p.a[PA_TOTALS][2] = NU;
   }
   __syncthreads();
 

@@ -21,7 +21,7 @@ namespace {
 
 // Scratch shared by every call on a device; held by each GPU that loads the
 // library until the process exits. 1 MiB covers every workload shape of the
-// tests (the largest, a 256-expert layer, needs about 194 KB).
+// tests (the largest, a 256-expert layer, needs about 200 KB).
 constexpr size_t kScratchBytes = 1u << 20;
 static __device__ __align__(256) uint8_t g_plan_scratch[kScratchBytes];
 
@@ -31,7 +31,8 @@ static __device__ __align__(256) uint8_t g_plan_scratch[kScratchBytes];
 // records, chunk counts per group, scale map) is written to the caller's output
 // buffer at its moe_plan_build offset.
 constexpr int kInternal[] = {PA_BITMAP,    PA_WPRE,     PA_NB,         PA_RANK_NB,
-                             PA_BAND_TILE, PA_SEG_GIDX, PA_GROUP_NSEG, PA_RANK_TILES};
+                             PA_BAND_TILE, PA_SEG_GIDX, PA_GROUP_NSEG, PA_RANK_TILES,
+                             PA_UNIT_TMP};
 
 constexpr int kMaxDevices = 64;
 // Device address of g_plan_scratch per device ordinal, looked up by the first
