@@ -563,6 +563,11 @@ def gate_arm(args):
     }
 
 
+def _frac(nbytes, ms, peak_gbs):
+    """Fraction of the peak HBM rate that nbytes in ms reach (None without a time)."""
+    return nbytes / (ms * 1e-3) / 1e9 / peak_gbs if ms and ms > 0 else None
+
+
 def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     """Per-kernel times of one step, and the producer alone on every SM (serial mode)."""
     import torch
@@ -606,6 +611,9 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         t = lay2.timings()
         for i, name in enumerate(["route", "plan", "producer", "consumer", "scale", "gather"]):
             ser.setdefault(name, []).append(t[i])
+        # Device-clock spans of the same launches (the means over the records so far;
+        # the last iteration's values are the means over all of them).
+        ser_span = {"producer": t[6], "scale": t[7], "consumer": t[10], "gather": t[11]}
     ser = {n: statistics.median(v) for n, v in ser.items()}
     del flush
     # Whole-step time of each schedule: consumer CTAs beside the producer (-1 fused,
@@ -697,6 +705,12 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         "scale_frac": scale_bytes / (ser["scale"] * 1e-3) / 1e9 / hbm,
         "gather_gbs": gather_bytes / (ser["gather"] * 1e-3) / 1e9,
         "gather_frac": gather_bytes / (ser["gather"] * 1e-3) / 1e9 / hbm,
+        "serial_span_ms": ser_span,
+        "consumer_standalone_span_frac": _frac(cons_bytes, ser_span["consumer"], hbm),
+        "scale_span_frac": _frac(scale_bytes, ser_span["scale"], hbm),
+        "gather_span_frac": _frac(gather_bytes, ser_span["gather"], hbm),
+        "span_timing": ("device clock, first CTA start to last CTA end, mean over the serial "
+                        "iterations (no launch latency, unlike the CUDA events)"),
         "hbm_stage_timing": ("serial schedule, CUDA events around each kernel, L2 flushed "
                              "(512 MB write, then read) before the routing, the plan build (the gather "
                              "is its last kernel), the producer and the scale; the consumer "

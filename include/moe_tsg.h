@@ -322,10 +322,11 @@ int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count)
  * [2] producer, [3] consumer, [4] scale, [5] gather only. Then, from the device clock,
  * means over the last 64 combines: [6] the producer's execution span (its first CTA's
  * start to its last CTA's end; unlike [2] it excludes time spent queued behind other
- * kernels, for example those of another batch in flight), [7] the span of
- * moe_scale_gated, [8] the part of [7] before the producer's end, [9] the span of
- * moe_gate. A slot with no
- * measurement is -1. Instrumentation only: moe_set_timing(plan, 1) records the events
+ * kernels, for example those of another batch in flight, and the launch latency CUDA
+ * events include), [7] the span of the scale (moe_scale or moe_scale_gated) after the
+ * combine, [8] the part of [7] before the producer's end, [9] the span of moe_gate,
+ * [10] the span of the consumer kernel (not the fused copy warp), [11] the span of the
+ * layout gather of moe_plan_build. A slot with no measurement is -1. Instrumentation only: moe_set_timing(plan, 1) records the events
  * and the device-clock records, 2 only the device-clock records (no CUDA event enters
  * the streams, so kernels keep overlapping as without timing), 0 nothing; enabling
  * resets the counts. */

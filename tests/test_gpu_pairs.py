@@ -197,6 +197,36 @@ def test_device_clock_records_of_an_overlapped_step():
     layer.close()
 
 
+@pytest.mark.parametrize("mode", ["overlap", "serial", "fused"])
+def test_device_clock_spans_of_every_kernel(mode):
+    """Timing mode 2 records each kernel's span (first CTA start to last CTA end): the
+    producer, the consumer kernel (none in the fused schedule, whose copy runs inside
+    the producer), the scale and the layout gather; outputs are unchanged by it."""
+    wl = get_workload("a100_like", T=1024)
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode=mode, consumer_ctas=8, canaries=False)
+    ref = [t.clone() for t in layer.out]
+    layer.set_timing(2)
+    sp, sc = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    for _ in range(3):
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                      producer=sp, consumer=None if mode == "serial" else sc)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    t = layer.timings()
+    assert len(t) == 12 and all(v == -1 for v in t[:6]), t
+    assert t[6] > 0 and t[7] > 0 and t[11] > 0, t
+    assert t[9] == -1, t  # no gate
+    if mode == "fused":
+        assert t[10] == -1, t
+    else:
+        assert t[10] > 0, t
+    if mode == "serial":  # one stream: the scale starts after the producer has ended
+        assert t[8] == 0, t
+    assert all(torch.equal(a, b) for a, b in zip(ref, layer.out))
+    layer.close()
+
+
 def test_gated_scale_device_wait_timeout_is_reported_and_recoverable():
     wl = get_workload("a100_like")
     inp = P.inputs_for(wl)

@@ -467,8 +467,13 @@ int moe_plan_build(moe_plan* p, const int32_t* ids, const void* const* x, moe_st
     CUDA_TRY(cudaMemsetAsync(p->plan_ws + p->offsets[PA_XPREV], 0xFE, p->counts[PA_XPREV] * 4, s));
     p->xprev_ready = true;
   }
+  DevPlan gp = dp;
+  if (p->spans) {  // the gather's span goes to the record of the combine that follows
+    gp.span = span_record(p, p->nspan);
+    CUDA_TRY(cudaMemsetAsync(gp.span + kSpanGatherStart, 0, 2 * sizeof(unsigned long long), s));
+  }
   tstart(p, kTGather, s);
-  CUDA_TRY(launch_gather(dp, xs, xb, p->num_sms, s));
+  CUDA_TRY(launch_gather(gp, xs, xb, p->num_sms, s));
   tstop(p, kTGather, s);
   tstop(p, kTPlan, s);
   return MOE_OK;
@@ -571,6 +576,8 @@ int moe_scale(moe_plan* p, const float* topk_w, const void* const* recv, void* c
   ScaleArgs a;
   std::memset(&a, 0, sizeof(a));
   a.p = dev_plan(p);
+  // Its span goes to the record of the last combine (whose words it zeroed).
+  if (p->spans && p->last_span >= 0) a.p.span = span_record(p, p->last_span);
   a.w = topk_w;
   for (int r = 0; r < d.W; ++r) {
     if (!aligned16(recv[r]) || !aligned16(out[r])) return MOE_ERR_ARG;
@@ -729,8 +736,9 @@ int moe_timings(moe_plan* p, float* ms, int n) {
     }
     ms[i] = (float)(sum / m);
   }
-  // Device-clock records: [6] the producer's span, [7] the overlapped scale's span,
-  // [8] the part of that span before the producer's end (means over the records).
+  // Device-clock records: [6] the producer's span, [7] the scale's span (moe_scale or
+  // moe_scale_gated), [8] the part of that span before the producer's end (means over
+  // the records).
   for (int i = kTSlots; i < n && i < kTSlots + 4; ++i) ms[i] = -1.f;
   const int m = std::min(p->nspan, kSpanRing);
   if (n > kTSlots && m > 0) {
@@ -755,26 +763,29 @@ int moe_timings(moe_plan* p, float* ms, int n) {
     if (nscale > 0 && n > kTSlots + 1) ms[kTSlots + 1] = (float)(scale / nscale);
     if (nscale > 0 && n > kTSlots + 2) ms[kTSlots + 2] = (float)(beside / nscale);
   }
-  // [9] the gate's span (first CTA start to last CTA end), over the records that hold one;
-  // the record a gate writes is that of the combine that follows it.
-  if (n > kTSlots + 3) {
-    ms[kTSlots + 3] = -1.f;
+  // [9] the gate's span, [10] the consumer kernel's, [11] the layout gather's (first CTA
+  // start to last CTA end), each over the records that hold one. The gate and the
+  // gather write the record of the combine that follows them.
+  for (int i = kTSlots + 3; i < n && i < kTSlots + 6; ++i) ms[i] = -1.f;
+  if (n > kTSlots + 3 && p->spans) {
     const int mg = std::min(p->nspan + 1, kSpanRing);
-    if (p->spans && mg > 0) {
-      CUDA_TRY(cudaDeviceSynchronize());
-      unsigned long long ring[kSpanWords * kSpanRing];
-      CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
-                          cudaMemcpyDeviceToHost));
-      double gate = 0.0;
-      int ngate = 0;
+    CUDA_TRY(cudaDeviceSynchronize());
+    unsigned long long ring[kSpanWords * kSpanRing];
+    CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
+                        cudaMemcpyDeviceToHost));
+    const int w0[3] = {kSpanGateStart, kSpanConsStart, kSpanGatherStart};
+    const int w1[3] = {kSpanGateEnd, kSpanConsEnd, kSpanGatherEnd};
+    for (int k = 0; k < 3 && kTSlots + 3 + k < n; ++k) {
+      double sum = 0.0;
+      int cnt = 0;
       for (int j = 0; j < mg; ++j) {
         const unsigned long long* r = ring + (size_t)kSpanWords * ((p->nspan - j) % kSpanRing);
-        if (r[kSpanGateEnd] != 0 && r[kSpanGateStart] != 0) {
-          gate += (double)(r[kSpanGateEnd] - ~r[kSpanGateStart]) * 1e-6;
-          ++ngate;
+        if (r[w1[k]] != 0 && r[w0[k]] != 0) {
+          sum += (double)(r[w1[k]] - ~r[w0[k]]) * 1e-6;
+          ++cnt;
         }
       }
-      if (ngate > 0) ms[kTSlots + 3] = (float)(gate / ngate);
+      if (cnt > 0) ms[kTSlots + 3 + k] = (float)(sum / cnt);
     }
   }
   return MOE_OK;

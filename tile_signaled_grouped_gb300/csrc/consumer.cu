@@ -36,8 +36,11 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   allow_dependent_launch();  // a scale launched behind this kernel may start beside it
   ConsumerSmem& sm =
       *reinterpret_cast<ConsumerSmem*>(smem_raw + (size_t)kChunkSlots * kChunkBytes);
+  if (threadIdx.x == 0) span_begin(a.p.span, kSpanConsStart);
   combine_copy<kChunkSlots, kLoadsInFlight>(a.p, a.y, a.recv, smem_raw, sm, blockIdx.x,
                                             gridDim.x);
+  __syncwarp();
+  if (threadIdx.x == 0) span_end(a.p.span, kSpanConsEnd);
 }
 
 }  // namespace

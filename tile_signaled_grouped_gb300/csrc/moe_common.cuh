@@ -33,15 +33,19 @@ constexpr int kMaxSegChunks = 256;           // copy chunks one segment may have
 constexpr int kSpanRing = 64;                // per-combine device-clock records kept while timing
 // One record of the span ring: eight u64 device-clock stamps (ns) of one combine.
 enum SpanWord {
-  kSpanProdStart = 0,   // ~(first producer CTA start), folded in with atomicMax
-  kSpanProdEnd = 1,     // last producer CTA end
-  kSpanScaleStart = 2,  // ~(first CTA start) of the overlapped scale
-  kSpanScaleEnd = 3,    // last CTA end of the overlapped scale
-  kSpanLastTile = 4,    // the producer's last finished output tile (its ready-flag release)
-  kSpanGateStart = 5,   // ~(first CTA start) of the gate before this combine
-  kSpanGateEnd = 6,     // last CTA end of that gate
-  kSpanCombineWords = 5,  // words [0, 5) are zeroed by each combine, [5, 7) by each gate
-  kSpanWords = 8
+  kSpanProdStart = 0,    // ~(first producer CTA start), folded in with atomicMax
+  kSpanProdEnd = 1,      // last producer CTA end
+  kSpanScaleStart = 2,   // ~(first CTA start) of the scale (moe_scale or moe_scale_gated)
+  kSpanScaleEnd = 3,     // last CTA end of the scale
+  kSpanLastTile = 4,     // the producer's last finished output tile (its ready-flag release)
+  kSpanConsStart = 5,    // ~(first CTA start) of the consumer kernel (not the fused copy warp)
+  kSpanConsEnd = 6,      // last CTA end of the consumer kernel
+  kSpanCombineWords = 7, // words [0, 7) are zeroed by each combine
+  kSpanGateStart = 7,    // ~(first CTA start) of the gate before this combine (zeroed by it)
+  kSpanGateEnd = 8,      // last CTA end of that gate
+  kSpanGatherStart = 9,  // ~(first CTA start) of the layout gather before this combine
+  kSpanGatherEnd = 10,   // last CTA end of that gather (both zeroed by the plan build)
+  kSpanWords = 12
 };
 
 // ---------------------------------------------------------------------------

@@ -661,6 +661,7 @@ __global__ void layout_gather_kernel(DevPlan p, const __grid_constant__ GatherPt
   }
   const int n16 = d.D / 8;
   const int warps = (gridDim.x * blockDim.x) >> 5;
+  if (threadIdx.x == 0) span_begin(p.span, kSpanGatherStart);
   for (int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; gw < total; gw += warps) {
     int o = 0;
 #pragma unroll
@@ -694,6 +695,10 @@ __global__ void layout_gather_kernel(DevPlan p, const __grid_constant__ GatherPt
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int c = lane; c < n16; c += 32) dst[c] = z;
     }
+  }
+  if (p.span != nullptr) {  // the same for the whole grid
+    __syncthreads();
+    if (threadIdx.x == 0) span_end(p.span, kSpanGatherEnd);
   }
 }
 

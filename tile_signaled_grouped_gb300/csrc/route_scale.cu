@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ Scal
   const int ntask = d.W * d.T * nblk;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (threadIdx.x == 0) span_begin(a.p.span, kSpanScaleStart);
   int src_n = INT_MIN;
   float w_n = 0.f;
   if (task < ntask && lane < d.k) {
@@ -132,6 +133,10 @@ __global__ void __launch_bounds__(256) scale_kernel(const __grid_constant__ Scal
     const int tok = task / nblk;
     scale_round<SG, CPL, false>(a, d, tok / d.T, tok % d.T, src_l, w_l, lane,
                                 (task % nblk) * 32 * CPL);
+  }
+  if (a.p.span != nullptr) {  // the same for the whole grid
+    __syncthreads();
+    if (threadIdx.x == 0) span_end(a.p.span, kSpanScaleEnd);
   }
 }
 

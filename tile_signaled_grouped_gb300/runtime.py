@@ -229,9 +229,9 @@ class ExpertCombine:
 
     def timings(self):
         """[route or gate, plan, producer, consumer, scale, gather, producer span,
-        gated-scale span, gated-scale time before the producer's end, gate span] in ms
-        (-1: none)."""
-        return capi.moe_timings(self.plan, 10)
+        scale span, scale time before the producer's end, gate span, consumer-kernel
+        span, gather span] in ms (-1: none)."""
+        return capi.moe_timings(self.plan, 12)
 
     def combine_overlap(self):
         """(share of the combine's bytes landed before the producer's last tile, µs from
