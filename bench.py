@@ -346,8 +346,8 @@ def gpu_arm(args, rank, world, local_rank):
                  "recv_rows": recv_rows},
         "timed_wall_s": wall,
         "device_clock_ms_in_timed_region": {
-            "producer_span": kernel_ms[6], "gated_scale_span": kernel_ms[7],
-            "gated_scale_before_producer_end": kernel_ms[8]},
+            "producer_span": kernel_ms[6], "scale_span": kernel_ms[7],
+            "scale_before_producer_end": kernel_ms[8]},
         # TileMoE notes 7.3: how much of the second all-to-all the FFN hides. Here: the
         # share of the combine's bytes whose copies had landed when the producer
         # finished its last output tile (last combine of the timed region).
