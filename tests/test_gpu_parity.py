@@ -54,6 +54,34 @@ def test_small_shapes_full_parity(wl):
     _full_check(wl, "overlap", cctas=4)
 
 
+# The producer's scheduling units keep an expert's run of tiles whole where it fits (at
+# most 32 tiles), cut longer runs into near-equal parts and pack short runs together.
+# long_runs: every expert's 48 remote tiles are cut into 24 + 24. mixed_runs (Zipf):
+# one rank has remote runs of 48, 29 and 20 tiles (units 24, 24, 29, 20), the other
+# 15, 11 and 9 (units 26, 9).
+UNIT_SHAPES = [
+    Workload("long_runs", W=4, L=1, topk=2, T=4096, d_model=128, d_ff=128, tb_M=128,
+             routing="balanced"),
+    Workload("mixed_runs", W=2, L=3, topk=2, T=8192, d_model=128, d_ff=128, tb_M=64,
+             routing="zipf"),
+]
+
+
+@pytest.mark.parametrize("pairs", [0, 1])
+@pytest.mark.parametrize("wl", UNIT_SHAPES, ids=lambda w: w.name)
+def test_scheduling_units_with_long_expert_runs(wl, pairs):
+    inp = P.inputs_for(wl)
+    layer = P.run_gpu(wl, inp, mode="overlap", consumer_ctas=4, pairs=pairs)
+    assert layer.status() == (0, 0)
+    orc = P.oracle_run(wl, inp)
+    P.check_plan(layer, wl, orc.plan, orc.ids, orc.w)
+    P.check_order(layer, wl, orc.plan)
+    if pairs:
+        P.check_pairs(layer, wl, orc.plan)
+    P.check_layout_and_outputs(layer, wl, inp, orc)
+    layer.close()
+
+
 @pytest.mark.parametrize("mode", ["overlap", "fused"])
 def test_largest_token_row(mode):
     """d_model = 10240, the largest the library takes: each copy chunk holds exactly one
