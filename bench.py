@@ -195,6 +195,12 @@ def gpu_arm(args, rank, world, local_rank):
     layers = [ExpertCombine(W, wl.L, k, T, D, F, wl.tb_M, wl.mgb, args.consumer_ctas,
                             producer_pairs=args.producer_pairs, scale_mode=args.scale)
               for _ in range(n_fly)]
+    # With batches in flight a batch's gate overlaps the previous batch's producer:
+    # for E <= 16 it takes CTAs that fit beside a producer CTA (MOE_GATE_BESIDE).
+    gate_splits = {"auto": capi.DEFINES["MOE_GATE_BESIDE"] if n_fly > 1 and wl.E <= 16 else 0,
+                   "default": 0, "beside": capi.DEFINES["MOE_GATE_BESIDE"]}[args.gate_shape]
+    for lay in layers:
+        lay.gate_splits = gate_splits
     layer = layers[0]
     sps = [torch.cuda.Stream() for _ in range(n_fly)]
     scs = [torch.cuda.Stream(priority=-1) for _ in range(n_fly)]
@@ -316,8 +322,10 @@ def gpu_arm(args, rank, world, local_rank):
                    else "one CTA per tile (M=128)",
                    "scale": ("overlapped with the producer (moe_scale_gated)"
                              if args.scale == "gated" else "after the combine (moe_scale)"),
-                   "routing": ("gate kernel from the token rows (seeded router)" if wr is not None
-                               else "from the drawn gate logits"),
+                   "routing": (("gate kernel from the token rows (seeded router), "
+                                + ("CTAs that fit beside the producer" if gate_splits < 0
+                                   else "moe_gate's own choice of CTAs"))
+                               if wr is not None else "from the drawn gate logits"),
                    "producer_ctas": launch[0], "consumer_ctas_launched": launch[1],
                    "num_sms": launch[2], "pair_clusters_resident": launch[3],
                    "parallelism": f"{W} logical EP ranks on 1 GPU; replicas x{world}",
@@ -860,6 +868,10 @@ def main():
                     help="after: moe_scale once the combine is done; gated: moe_scale_gated, "
                          "launched behind the producer, waits on the device for each token's "
                          "group signals and ready flags")
+    ap.add_argument("--gate-shape", default="auto", choices=["auto", "default", "beside"],
+                    help="with --route gate: moe_gate's own choice (default, splits 0) or, for "
+                         "E <= 16, CTAs that fit beside a producer CTA (beside); auto: beside "
+                         "with batches in flight")
     ap.add_argument("--route", default="logits", choices=["logits", "gate"],
                     help="logits: route from the drawn gate logits; gate: the gate kernel scores "
                          "the token rows with a seeded router (softmax and top-k in the same "

@@ -51,6 +51,10 @@ typedef struct CUstream_st *moe_stream_t;
 /* moe_cfg.consumer_ctas value: the combine copy runs inside the pair producer. */
 #define MOE_CONSUMER_FUSED (-1)
 
+/* moe_gate splits value: for E <= 16, CTAs small enough to share an SM with a running
+ * producer CTA (a gate that runs beside the previous batch's combine). */
+#define MOE_GATE_BESIDE (-1)
+
 enum moe_error {
   MOE_OK = 0,
   MOE_ERR_ARG = -1,         /* invalid configuration or argument */
@@ -134,13 +138,19 @@ int moe_route(moe_plan *plan, const float *logits, const int32_t *forced_ids,
  *  splits:     0 picks the kernel: for E <= 16 one that streams the token rows
  *              from HBM into registers and takes the scores with mma.sync (the
  *              contraction is 8 or 16 columns wide and the launch a one-shot read
- *              of x); above, the tcgen05 kernel with the K split it picks. 1, 2, 4
- *              or 8 force the tcgen05 kernel with that split (that many CTAs of one
- *              cluster share a 128-token tile, each summing a range of D).
+ *              of x), in CTAs of 32 tokens and 8 warps (16 tokens and 4 warps with
+ *              9-16 experts) when there are enough of them to fill every SM, else in
+ *              larger CTAs that spread the tokens over one wave; above, the tcgen05
+ *              kernel with the K split it picks. 1, 2, 4 or 8 force the tcgen05
+ *              kernel with that split (that many CTAs of one cluster share a
+ *              128-token tile, each summing a range of D).
+ *              MOE_GATE_BESIDE: for E <= 16 always the small CTAs, which fit in what a
+ *              pair-producer CTA leaves of its SM, so the gate of the next batch runs
+ *              beside a running combine instead of waiting for its SMs; above, as 0.
  * Both kernels add each score's partial sums in a fixed order, so a given choice
  * gives the same bits on every call; the two kernels' scores differ by rounding
  * only. A tcgen05 tile holds as many tokens (a multiple of 8, at most 128) as fill
- * one wave of CTAs, and so does a CTA of the other kernel (at most 128 tokens).
+ * one wave of CTAs.
  * The routing tail also sets the plan's token bitmaps (prescribed ids out of range
  * or repeated set MOE_DEV_ROUTING), for a following moe_plan_build(plan, NULL, ...).
  * E <= 256; larger E, or a split the GPU cannot hold, gives MOE_ERR_UNSUPPORTED.

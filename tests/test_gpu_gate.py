@@ -156,10 +156,32 @@ ROWS_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("splits", [0, capi.DEFINES["MOE_GATE_BESIDE"]], ids=["wave", "beside"])
 @pytest.mark.parametrize("wl", ROWS_SHAPES, ids=lambda w: w.name)
-def test_rows_gate_parity(wl):
-    ids_g, w_g, lg_g, xs, wr, _ = run_gate(wl)
+def test_rows_gate_parity(wl, splits):
+    """splits 0: the small CTAs where they fill every SM (rows_E9_T2500, rows_E8_waves),
+    else CTAs that spread the tokens over one wave; MOE_GATE_BESIDE: always the small
+    CTAs that fit beside a producer CTA (32 tokens, 8 warps; 16 tokens, 4 warps with
+    two n-tiles)."""
+    ids_g, w_g, lg_g, xs, wr, _ = run_gate(wl, splits)
     check_gate(wl, xs, wr, ids_g, w_g, lg_g)
+
+
+@pytest.mark.parametrize("T", [1024, 4096])
+def test_gate_small_and_wave_ctas(T):
+    """A100-like layer (4 ranks, E = 8). T = 1024: 128 small CTAs would not fill the
+    GPU, so splits 0 spreads the tokens over one wave of larger CTAs while
+    MOE_GATE_BESIDE keeps the small ones; both pass the feasibility check against the
+    oracle (their scores differ by summation order only). T = 4096: both take the
+    small CTAs, and give the same scores, ids and weights bit for bit."""
+    wl = get_workload("a100_like", routing="gate", T=T)
+    a = run_gate(wl, 0)
+    b = run_gate(wl, capi.DEFINES["MOE_GATE_BESIDE"])
+    check_gate(wl, a[3], a[4], a[0], a[1], a[2])
+    check_gate(wl, b[3], b[4], b[0], b[1], b[2])
+    if T == 4096:
+        for x, y in zip(a[:3], b[:3]):
+            assert np.array_equal(x, y)
 
 
 @pytest.mark.parametrize("name", ["a100_like", "qwen3_235b_like", "deepseek_v3_like",

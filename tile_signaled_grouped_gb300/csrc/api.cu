@@ -372,14 +372,20 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
   if (p == nullptr || x == nullptr || !aligned16(w_router) || !null_or_aligned16(forced) ||
       !aligned16(ids) || !aligned16(w) || !null_or_aligned16(logits))
     return MOE_ERR_ARG;
-  if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8) return MOE_ERR_ARG;
+  if (splits != MOE_GATE_BESIDE && splits != 0 && splits != 1 && splits != 2 && splits != 4 &&
+      splits != 8)
+    return MOE_ERR_ARG;
   const Dims& d = p->d;
   for (int r = 0; r < d.W; ++r)
     if (!aligned16(x[r])) return MOE_ERR_ARG;
+  // MOE_GATE_BESIDE with E <= 16: the rows kernel in CTAs that fit beside a producer
+  // CTA; with larger E the tcgen05 kernel as with splits == 0 (its CTAs cannot).
+  const bool beside = splits == MOE_GATE_BESIDE;
+  if (beside) splits = 0;
   const int lg = splits == 8 ? 3 : splits == 4 ? 2 : splits == 2 ? 1 : 0;
   if (p->gate_npad == 0 || (splits != 0 && p->gate_clusters[lg] == 0)) return MOE_ERR_UNSUPPORTED;
-  // splits == 0 with E <= 16 (and a router that fits in shared memory): the kernel
-  // that streams the token rows into registers; otherwise the tcgen05 kernel.
+  // splits == 0 with E <= 16: the kernel that streams the token rows into registers;
+  // otherwise the tcgen05 kernel.
   const bool rows_kernel = splits == 0 && gate_rows_fits(d.E, d.D);
   GateArgs ga{};
   GateRowsArgs ra{};
@@ -391,7 +397,7 @@ int moe_gate(moe_plan* p, const void* const* x, const void* w_router, const int3
     ra.w = w;
     ra.logits = logits;
     ra.p = dev_plan(p);
-    gate_rows_shape(d.W, d.T, d.E, d.D, p->num_sms, &ra.rows, &ra.kslices);
+    gate_rows_shape(d.W, d.T, d.E, d.D, p->num_sms, beside, &ra.rows, &ra.kslices);
   } else {
     ga.npad = p->gate_npad;
     ga.forced = forced;

@@ -35,9 +35,11 @@
 // thread's long dependent chain) and sets the plan's token bitmap bits from the ids it
 // holds; prescribed ids go through a thread per token and the plan build's checks.
 //
-// Grid. CTA j of rank s takes tokens [j rows, (j + 1) rows) of that rank, rows chosen
-// (gate_rows_shape) so that the W ranks' CTAs fill one wave of SMs; a CTA has
-// ceil(rows / 16) groups x kslices warps, at most 32 (16 with two n-tiles). The kernel
+// Grid. CTA j of rank s takes tokens [j rows, (j + 1) rows) of that rank; a CTA has
+// ceil(rows / 16) groups x kslices warps. gate_rows_shape picks small CTAs (32 tokens
+// and 8 warps, or 16 and 4 with two n-tiles) that fit beside a producer CTA and, with
+// enough tokens, fill an idle GPU as well; with few tokens, CTAs of up to 128 tokens
+// and 32 warps (16 with two n-tiles) that spread them over one wave of SMs. The kernel
 // has no wait but its two CTA barriers.
 #include "moe_common.cuh"
 #include "route_topk.cuh"
@@ -249,9 +251,25 @@ cudaError_t preload_gate_rows() { return cudaSuccess; }
 
 bool gate_rows_fits(int E, int D) { return E >= 1 && E <= 16 && D % 64 == 0; }
 
-void gate_rows_shape(int W, int T, int E, int D, int num_sms, int* rows, int* kslices) {
-  // As many tokens per CTA as make the W ranks' CTAs one wave (at most 128), then as
-  // many K slices per 16-token group as the CTA's warps allow (at least one step each).
+void gate_rows_shape(int W, int T, int E, int D, int num_sms, bool beside, int* rows,
+                     int* kslices) {
+  // Small CTAs: a pair-producer CTA leaves about 25 K registers and 11 KB of shared
+  // memory of its SM, room for 8 warps of 64 registers (one n-tile) or 4 of 104 (two)
+  // with 6 KB of partials: two 16-token groups (one with two n-tiles) of up to 4 K
+  // slices. On an idle GPU up to four of them share an SM, which keeps more loads in
+  // flight than one wave-filling CTA and evens out the SMs' ends, so they are also the
+  // automatic choice whenever there are enough of them to fill every SM once.
+  const int small_ks = std::max(1, std::min(4, D / 64));
+  const int small_groups = std::max(1, (rows_nt(E) == 1 ? 8 : 4) / small_ks);
+  const int small_rows = std::min(T, 16 * small_groups);
+  if (beside || (long long)W * ((T + small_rows - 1) / small_rows) >= num_sms) {
+    *rows = small_rows;
+    *kslices = small_ks;
+    return;
+  }
+  // Otherwise as many tokens per CTA as make the W ranks' CTAs one wave (at most 128),
+  // then as many K slices per 16-token group as the CTA's warps allow (at least one
+  // step each).
   const int per_rank = std::max(1, num_sms / std::max(1, W));
   const int r = std::min(kRowsMaxTokens, std::max(1, (T + per_rank - 1) / per_rank));
   const int groups = (r + 15) / 16;

@@ -178,8 +178,10 @@ cudaError_t preload_gate_rows();
 // Whether the kernel takes E experts of D columns (E <= 16, its router and partial
 // sums in shared memory).
 bool gate_rows_fits(int E, int D);
-// Tokens per CTA and K slices for T tokens per rank on W ranks and num_sms SMs.
-void gate_rows_shape(int W, int T, int E, int D, int num_sms, int* rows, int* kslices);
+// Tokens per CTA and K slices for T tokens per rank on W ranks and num_sms SMs; with
+// `beside`, CTAs small enough to share an SM with a running producer CTA.
+void gate_rows_shape(int W, int T, int E, int D, int num_sms, bool beside, int* rows,
+                     int* kslices);
 cudaError_t launch_gate_rows(const GateRowsArgs& a, cudaStream_t s);
 
 struct ProducerArgs {

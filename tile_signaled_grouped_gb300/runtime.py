@@ -31,6 +31,10 @@ class ExpertCombine:
         if scale_mode not in ("after", "gated"):
             raise ValueError(f"scale_mode {scale_mode!r}")
         self.scale_mode = scale_mode
+        # The moe_gate splits argument of forward() and HostPipeline steps routed from a
+        # router: 0 picks the kernel; MOE_GATE_BESIDE (E <= 16) takes CTAs that fit
+        # beside a running producer, for batches in flight.
+        self.gate_splits = 0
         self.device = torch.device(device or "cuda")
         self.cfg = capi.moe_cfg(W, L, topk, T, d_model, d_ff, tb_M, mgb, consumer_ctas,
                                 timeout_ns, producer_pairs)
@@ -139,7 +143,7 @@ class ExpertCombine:
         if (logits is None) == (w_router is None):
             raise ValueError("give exactly one of logits and w_router")
         if w_router is not None:
-            self.gate(x, w_router, forced_ids, producer)
+            self.gate(x, w_router, forced_ids, producer, splits=self.gate_splits)
         else:
             self.route(logits, forced_ids, producer)
         self.plan_build(x, stream=producer, from_gate=w_router is not None)
@@ -313,7 +317,7 @@ class HostPipeline:
         sp.wait_event(self.ev_in[b])
         fid = self.forced[b] if hforced is not None else None
         if w_router is not None:
-            lay.gate(self.x[b], w_router, fid, sp)
+            lay.gate(self.x[b], w_router, fid, sp, splits=lay.gate_splits)
         else:
             lay.route(self.logits[b], fid, sp)
         lay.plan_build(self.x[b], stream=sp, from_gate=w_router is not None)
