@@ -31,8 +31,8 @@
 // Sums. Each warp's accumulator is a 16 x 8NT fp32 partial of its K slice (the MMA's C
 // fragment), written to shared memory; after the CTA barrier each token's scores are
 // its group's partials added in slice order (a fixed order: the same bits on every
-// call). An octet of lanes routes a token (route_octet: butterflies instead of one
-// thread's long dependent chain) and sets the plan's token bitmap bits from the ids it
+// call). An octet of lanes routes a token (route_lanes<8, NT>: butterflies instead of
+// one thread's long dependent chain) and sets the plan's token bitmap bits from the ids it
 // holds; prescribed ids go through a thread per token and the plan build's checks.
 //
 // Grid. CTA j of rank s takes tokens [j rows, (j + 1) rows) of that rank; a CTA has
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(rows_max_warps(NT) * 32, 1)
     return v;
   };
   if (a.forced == nullptr) {
-    // The gate's own top k: an octet of lanes per token (route_octet), lane li holding
+    // The gate's own top k: an octet of lanes per token (route_lanes), lane li holding
     // experts li and li + 8.
     constexpr int PER = NT;
     const int li = lane & 7;
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(rows_max_warps(NT) * 32, 1)
       }
       const TokenMark mk{reinterpret_cast<uint32_t*>(a.p.a[PA_BITMAP]), (size_t)d.W * d.TW,
                          (size_t)s * d.TW + (t >> 5), 1u << (t & 31)};
-      route_octet<PER>(v, d.k, a.ids + tok * d.k, a.w + tok * d.k, li, active, &mk);
+      route_lanes<8, PER>(v, d.k, a.ids + tok * d.k, a.w + tok * d.k, li, active, &mk);
     }
   } else {
     // Prescribed ids: a thread per token, the ids checked and marked (mark_token).

@@ -1,5 +1,5 @@
-// Routing of one token by a warp, by the 8 lanes of an octet or by one thread: softmax
-// over its E gate scores and the top k.
+// Routing of one token by a warp, by a group of lanes or by one thread: softmax over
+// its E gate scores and the top k.
 //
 // TileMoE notes (zhongzhuzhou.org), section 2.1 and 2.2 step 1: the router turns a
 // token's scores into a probability distribution over the E experts and keeps the
@@ -208,56 +208,66 @@ __device__ __forceinline__ void route_group(const float (&vin)[PER], int E, int 
   }
 }
 
-// One token routed by the 8 lanes of an octet (lanes 8o .. 8o + 7 of a converged
-// warp; the warp's four octets route four tokens at once). Lane li holds the scores of
-// experts li + 8i (PER of them, -inf past E), k <= E. The decision and the weights are
-// route_group's: larger score first, equal scores to the lower id; weight = the
-// softmax probability at the chosen id. The maximum, the sum of the exponentials and
-// each round's winner are butterflies over the octet (xor 4, 2, 1); fp32 addition and
-// the (score, id) order are commutative, so every lane of the octet ends with the same
-// values. Where a thread per token runs a chain of some hundred dependent steps, the
-// octet runs a dozen shuffles. Lane 0 of an active octet writes slot j (and, with
-// `mark`, the token's bit of that expert).
-template <int PER>
-__device__ __forceinline__ void route_octet(const float (&vin)[PER], int k, int32_t* ids_row,
-                                            float* w_row, int li, bool active,
+// One token routed by a group of G lanes (G = 2, 4, 8, 16 or 32 consecutive lanes of a
+// converged warp, aligned to G; the warp's 32 / G groups route as many tokens at once).
+// Lane lig of the group holds the scores of experts lig + G i (PER <= 8 of them, -inf
+// past E), k <= E. The decision and the weights are route_group's: larger score first,
+// equal scores to the lower id; weight = the softmax probability at the chosen id.
+// The maximum, the sum of the exponentials and each round's winner are butterflies
+// over the group (xor G/2, ..., 1); fp32 addition and the (score, id) order are
+// commutative, so every lane of the group ends with the same values. Each lane sorts
+// its candidates once (route_sort), so a round compares the groups' heads and the
+// winner's lane shifts its list: where a thread per token runs a chain of some
+// hundred dependent steps, or a warp per token a chain of redux.sync rounds for one
+// token at a time, a group runs log2 G shuffles per round for 32 / G tokens at once.
+// Lane 0 of an active group writes slot j (and, with `mark`, the token's bit of that
+// expert).
+template <int G, int PER>
+__device__ __forceinline__ void route_lanes(const float (&vin)[PER], int k, int32_t* ids_row,
+                                            float* w_row, int lig, bool active,
                                             const TokenMark* mark) {
+  static_assert(G == 2 || G == 4 || G == 8 || G == 16 || G == 32, "lanes per token");
+  static_assert(PER >= 1 && PER <= 8, "candidates per lane");
   constexpr uint32_t kAll = 0xFFFFFFFFu;
   float mx = vin[0];
 #pragma unroll
   for (int i = 1; i < PER; ++i) mx = fmaxf(mx, vin[i]);
 #pragma unroll
-  for (int o = 4; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, o));
+  for (int o = G / 2; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, o));
   float sum = 0.f;
 #pragma unroll
   for (int i = 0; i < PER; ++i) sum += expf(vin[i] - mx);
 #pragma unroll
-  for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(kAll, sum, o);
+  for (int o = G / 2; o; o >>= 1) sum += __shfl_xor_sync(kAll, sum, o);
   const float inv = 1.0f / sum;
-  uint32_t key[PER];
+  float v[PER];
+  int e[PER];
 #pragma unroll
-  for (int i = 0; i < PER; ++i) key[i] = float_key(vin[i]);
-  uint32_t taken = 0;  // bit i: this lane's candidate i already chosen
+  for (int i = 0; i < PER; ++i) {
+    v[i] = vin[i];
+    e[i] = lig + G * i;
+  }
+  route_sort<PER>(v, e);
+  int left = PER;  // candidates not yet taken, at the head of the sorted list
   for (int j = 0; j < k; ++j) {
-    // This lane's best candidate not yet taken (key 0: none; every score has a key > 0).
-    uint32_t bk = 0, be = 0xFFFFFFFFu;
+    // This lane's head (key 0: none left; every score has a key > 0), then the group's.
+    uint32_t bk = left > 0 ? float_key(v[0]) : 0u;
+    uint32_t be = left > 0 ? (uint32_t)e[0] : 0xFFFFFFFFu;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const uint32_t e = (uint32_t)(li + 8 * i);
-      const bool better = !((taken >> i) & 1u) & ((key[i] > bk) | ((key[i] == bk) & (e < be)));
-      bk = better ? key[i] : bk;
-      be = better ? e : be;
-    }
-#pragma unroll
-    for (int o = 4; o; o >>= 1) {
+    for (int o = G / 2; o; o >>= 1) {
       const uint32_t ok = __shfl_xor_sync(kAll, bk, o), oe = __shfl_xor_sync(kAll, be, o);
       const bool take = (ok > bk) | ((ok == bk) & (oe < be));
       bk = take ? ok : bk;
       be = take ? oe : be;
     }
+    const bool win = left > 0 && (uint32_t)e[0] == be;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) taken |= ((uint32_t)(li + 8 * i) == be) ? 1u << i : 0u;
-    if (active && li == 0) {
+    for (int i = 0; i + 1 < PER; ++i) {
+      v[i] = win ? v[i + 1] : v[i];
+      e[i] = win ? e[i + 1] : e[i];
+    }
+    left -= win ? 1 : 0;
+    if (active && lig == 0) {
       ids_row[j] = (int32_t)be;
       w_row[j] = expf(key_float(bk) - mx) * inv;
       if (mark != nullptr) atomicOr(mark->bitmap + be * mark->per_expert + mark->word, mark->bit);
