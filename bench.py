@@ -693,7 +693,10 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     flops = 6.0 * rows * D * wl.d_ff
     cons_bytes = 4.0 * D * sum(recv_rows)
     scale_bytes = 2.0 * D * k * W * T + 2.0 * D * W * T + 8.0 * W * T * k
-    gather_bytes = 2.0 * D * (valid + rows)
+    # The layout gather's least DRAM traffic: every token row read once (its k copies in
+    # X come from the same source row) and every valid X row written; zero rows that
+    # were already zero after the previous gather are not rewritten.
+    gather_bytes = 2.0 * D * (W * T + valid)
     lay2.close()
     return {
         "overlapped_ms": over,

@@ -640,8 +640,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
 
 // Layout gather: X rows of every owner from its tokens' rows, zero rows elsewhere
 // (padding, block tails, and up to the next 128-row boundary). One warp per row,
-// over the rows that exist (their count is read on the device); each lane keeps
-// up to 8 independent 16-byte loads in flight. A row that is to be zero and was
+// over the rows that exist (their count is read on the device); a warp reads the
+// plan entries of 32 of its rows at once, and each lane keeps up to 8 independent
+// 16-byte loads of a row in flight. A row that is to be zero and was
 // already zero after the previous gather (PA_XPREV) is left alone: padding-heavy
 // layouts keep most of their zero rows from one step to the next.
 struct GatherPtrs {
@@ -662,38 +663,53 @@ __global__ void layout_gather_kernel(DevPlan p, const __grid_constant__ GatherPt
   const int n16 = d.D / 8;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   if (threadIdx.x == 0) span_begin(p.span, kSpanGatherStart);
-  for (int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; gw < total; gw += warps) {
-    int o = 0;
+  // A warp takes rows gw, gw + warps, ... in batches of 32: lane j reads the plan
+  // entries of the batch's j-th row (one round trip for 32 rows), and the warp then
+  // copies or zeroes, one row at a time, only the rows that need it.
+  for (int base = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; base < total;
+       base += 32 * warps) {
+    const int gw = base + lane * warps;
+    int o = 0, r = 0, src = -1;
+    bool work = false;
+    if (gw < total) {
 #pragma unroll
-    for (int q = 0; q < MOE_MAX_RANKS - 1; ++q) o += (q < d.W - 1 && gw >= end[q]) ? 1 : 0;
-    const int r = gw - (o > 0 ? end[o - 1] : 0);
-    const int rows = p.a[PA_RANK_ROWS][o];
-    const int src = r < rows ? p.a[PA_XSRC][(size_t)o * d.RM + r] : -1;
-    int32_t* prev = p.a[PA_XPREV] + (size_t)o * d.RM + r;
-    const int before = *prev;
-    uint4* dst = reinterpret_cast<uint4*>(g.xb[o] + (size_t)r * d.D);
-    if (src < 0 && before == -1) continue;  // still a zero row
-    __syncwarp();
-    if (lane == 0 && before != src) *prev = src;
-    if (src >= 0) {
-      const int s = src / d.T, t = src % d.T;
-      const uint4* sp = reinterpret_cast<const uint4*>(g.x[s] + (size_t)t * d.D);
-      for (int c0 = 0; c0 < n16; c0 += 8 * 32) {
-        uint4 v[8];
+      for (int q = 0; q < MOE_MAX_RANKS - 1; ++q) o += (q < d.W - 1 && gw >= end[q]) ? 1 : 0;
+      r = gw - (o > 0 ? end[o - 1] : 0);
+      const int rows = p.a[PA_RANK_ROWS][o];
+      src = r < rows ? p.a[PA_XSRC][(size_t)o * d.RM + r] : -1;
+      int32_t* prev = p.a[PA_XPREV] + (size_t)o * d.RM + r;
+      const int before = *prev;
+      work = !(src < 0 && before == -1);  // else still a zero row
+      if (before != src) *prev = src;
+    }
+    uint32_t todo = __ballot_sync(0xFFFFFFFFu, work);
+    while (todo) {
+      const int j = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int jo = __shfl_sync(0xFFFFFFFFu, o, j);
+      const int jr = __shfl_sync(0xFFFFFFFFu, r, j);
+      const int jsrc = __shfl_sync(0xFFFFFFFFu, src, j);
+      uint4* dst = reinterpret_cast<uint4*>(g.xb[jo] + (size_t)jr * d.D);
+      if (jsrc >= 0) {
+        const int s = jsrc / d.T, t = jsrc % d.T;
+        const uint4* sp = reinterpret_cast<const uint4*>(g.x[s] + (size_t)t * d.D);
+        for (int c0 = 0; c0 < n16; c0 += 8 * 32) {
+          uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = c0 + u * 32 + lane;
-          if (c < n16) v[u] = __ldg(sp + c);
+          for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < n16) v[u] = __ldg(sp + c);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < n16) dst[c] = v[u];
+          }
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = c0 + u * 32 + lane;
-          if (c < n16) dst[c] = v[u];
-        }
+      } else {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int c = lane; c < n16; c += 32) dst[c] = z;
       }
-    } else {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int c = lane; c < n16; c += 32) dst[c] = z;
     }
   }
   if (p.span != nullptr) {  // the same for the whole grid
