@@ -84,7 +84,8 @@ class ExpertCombine:
         optional [W, T, E] fp32 tensor that receives the scores. splits: 0 picks the
         kernel (for E <= 16 the one that streams the token rows into registers, else
         the tcgen05 kernel with the K split it picks); 1, 2, 4 or 8 force the tcgen05
-        kernel with that K split."""
+        kernel with that K split; capi.DEFINES["MOE_GATE_BESIDE"] (E <= 16) takes the
+        small CTAs that fit beside a running producer CTA."""
         capi.moe_gate(self.plan, [t.data_ptr() for t in x], w_router.data_ptr(),
                       None if forced_ids is None else forced_ids.data_ptr(),
                       self.ids.data_ptr(), self.w.data_ptr(),
