@@ -114,11 +114,28 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+def source_fingerprint(names) -> str:
+    """First 16 hex digits of the sha256 of the code of the named csrc files, with their
+    comments and blank lines left out (a change to a comment does not change a kernel)."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for f in names:
+        text = open(os.path.join(ROOT, "tile_signaled_grouped_gb300", "csrc", f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for line in text.splitlines():
+            code = re.sub(r"//.*", "", line).rstrip()
+            if code.strip():
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
 def producer_traffic(wl_name: str, reduced: bool, pairs: int):
     """DRAM bytes (read + write) per producer launch, from the committed ncu summary of the
-    A100-like full-size run of the producer in use, while its sources still hash to the
-    fingerprint recorded there; None otherwise (changed kernel, other workload)."""
-    import hashlib
+    A100-like full-size run of the producer in use, while its sources still have the
+    fingerprint recorded there (source_fingerprint); None otherwise (changed kernel, other
+    workload)."""
     import re
 
     if wl_name != WORKLOAD or reduced:
@@ -127,14 +144,12 @@ def producer_traffic(wl_name: str, reduced: bool, pairs: int):
                      else ("ffn_producer_a100_like.md", ("ffn.cu",)))
     try:
         text = open(os.path.join(ROOT, "profiles", summary)).read()
-        h = hashlib.sha256()
-        for f in srcs + ("moe_common.cuh",):
-            h.update(open(os.path.join(ROOT, "tile_signaled_grouped_gb300", "csrc", f), "rb").read())
+        fp = source_fingerprint(srcs + ("moe_common.cuh",))
     except OSError:
         return None
     m1 = re.search(r"traffic_bytes_per_launch: (\d+)", text)
     m2 = re.search(r"source_fingerprint: (\w+)", text)
-    if not (m1 and m2) or h.hexdigest()[:16] != m2.group(1):
+    if not (m1 and m2) or fp != m2.group(1):
         return None
     return int(m1.group(1))
 

@@ -175,8 +175,7 @@ struct GateRowsArgs {
   int kslices;  // warps sharing a 16-token group, each a contiguous range of 64 columns
 };
 cudaError_t preload_gate_rows();
-// Whether the kernel takes E experts of D columns (E <= 16, its router and partial
-// sums in shared memory).
+// Whether the kernel takes E experts of D columns (E <= 16, D a multiple of 64).
 bool gate_rows_fits(int E, int D);
 // Tokens per CTA and K slices for T tokens per rank on W ranks and num_sms SMs; with
 // `beside`, CTAs small enough to share an SM with a running producer CTA.
