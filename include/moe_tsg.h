@@ -230,6 +230,16 @@ int moe_scale_gated(moe_plan *plan, const float *topk_w, const void *const *recv
 int moe_combine_overlap(moe_plan *plan, double *landed_frac, double *tail_us,
                         double *copy_bytes);
 
+/* The device-clock intervals of the producer launches recorded while device-clock
+ * records were on (moe_set_timing 1 or 2), oldest first: start_ns[i], end_ns[i] are
+ * the i-th launch's first CTA start and last CTA end on the GPU's global timer
+ * (nanoseconds; comparable across the plans of one device, so a caller running
+ * several plans in turn can take the union of their launches). At most max_records of
+ * the last 64 launches; *count receives how many were written. Synchronises the
+ * device. MOE_ERR_ARG without records. */
+int moe_producer_spans(moe_plan *plan, unsigned long long *start_ns, unsigned long long *end_ns,
+                       int max_records, int *count);
+
 /* Plan build that allocates nothing, for callers that cannot call cudaMalloc (for
  * example a serving loop that reserved all of its device memory up front, or a
  * runtime whose device memory comes from an allocator it does not own). The pages

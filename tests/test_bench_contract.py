@@ -105,3 +105,29 @@ def test_clock_summary_keeps_the_timed_region_only(tmp_path):
     assert s["samples"] == 7 and s["window"] == "timed region"
     assert s["sm_mhz"] == 1400 and s["sm_max_mhz"] == 2070
     assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_producer_launch_time_counts_overlap_once():
+    """Launches of two batches in flight overlap: each moment of any producer running
+    counts once, and gaps between launches count not at all."""
+    ns = 1_000_000  # 1 ms in ns
+    one = [(0, 2 * ns)]
+    assert abs(bench.producer_launch_ms(one) - 2.0) < 1e-12
+    # two launches sharing 0.5 ms, then one after a gap: (2.5 + 1) ms busy over 3
+    spans = [(0, 2 * ns), (int(1.5 * ns), int(2.5 * ns)), (10 * ns, 11 * ns)]
+    assert abs(bench.producer_launch_ms(spans) - 3.5 / 3) < 1e-12
+    # order of the records does not matter; a launch inside another adds nothing
+    spans2 = [(10 * ns, 11 * ns), (int(0.5 * ns), ns), (0, 2 * ns)]
+    assert abs(bench.producer_launch_ms(spans2) - 3.0 / 3) < 1e-12
+
+
+def test_source_fingerprint_ignores_comments(tmp_path, monkeypatch):
+    csrc = tmp_path / "tile_signaled_grouped_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("int a = 1;  // one\n\n/* block\n comment */\nint b = 2;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    fp = bench.source_fingerprint(("k.cu",))
+    (csrc / "k.cu").write_text("// header\nint a = 1;\n\n\nint b = 2;  // two\n")
+    assert bench.source_fingerprint(("k.cu",)) == fp
+    (csrc / "k.cu").write_text("int a = 1;\nint b = 3;\n")
+    assert bench.source_fingerprint(("k.cu",)) != fp

@@ -82,6 +82,7 @@ def load():
         "moe_expert_combine": (ip, [vp, P(vp), P(vp), P(vp), P(vp), vp, vp]),
         "moe_scale": (ip, [vp, vp, P(vp), P(vp), vp]),
         "moe_scale_gated": (ip, [vp, vp, P(vp), P(vp), vp]),
+        "moe_producer_spans": (ip, [vp, P(ctypes.c_ulonglong), P(ctypes.c_ulonglong), ip, P(ip)]),
         "moe_combine_overlap": (ip, [vp, P(ctypes.c_double), P(ctypes.c_double),
                                      P(ctypes.c_double)]),
         "moe_status": (ip, [vp, vp, P(ip), P(ip)]),
@@ -175,6 +176,15 @@ def moe_scale(plan, topk_w, recv, out, stream):
 def moe_scale_gated(plan, topk_w, recv, out, stream):
     check(lib().moe_scale_gated(plan, topk_w, ptr_array(recv), ptr_array(out), stream),
           "moe_scale_gated")
+
+
+def moe_producer_spans(plan, max_records=64):
+    """[(start_ns, end_ns)] of the recorded producer launches, oldest first."""
+    s = (ctypes.c_ulonglong * max_records)()
+    e = (ctypes.c_ulonglong * max_records)()
+    n = ctypes.c_int()
+    check(lib().moe_producer_spans(plan, s, e, max_records, ctypes.byref(n)), "moe_producer_spans")
+    return [(s[i], e[i]) for i in range(n.value)]
 
 
 def moe_combine_overlap(plan):

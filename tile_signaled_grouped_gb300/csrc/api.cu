@@ -624,6 +624,25 @@ int moe_scale_gated(moe_plan* p, const float* topk_w, const void* const* recv, v
   return MOE_OK;
 }
 
+int moe_producer_spans(moe_plan* p, unsigned long long* start_ns, unsigned long long* end_ns,
+                       int max_records, int* count) {
+  if (p == nullptr || start_ns == nullptr || end_ns == nullptr || count == nullptr ||
+      max_records < 0 || !p->spans)
+    return MOE_ERR_ARG;
+  CUDA_TRY(cudaDeviceSynchronize());
+  unsigned long long ring[kSpanWords * kSpanRing];
+  CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
+                      cudaMemcpyDeviceToHost));
+  const int m = std::min(std::min(p->nspan, kSpanRing), max_records);
+  for (int i = 0; i < m; ++i) {  // oldest first
+    const unsigned long long* r = ring + (size_t)kSpanWords * ((p->nspan - m + i) % kSpanRing);
+    start_ns[i] = ~r[kSpanProdStart];
+    end_ns[i] = r[kSpanProdEnd];
+  }
+  *count = m;
+  return MOE_OK;
+}
+
 int moe_combine_overlap(moe_plan* p, double* landed_frac, double* tail_us, double* copy_bytes) {
   if (p == nullptr || !p->spans || p->last_span < 0) return MOE_ERR_ARG;
   CUDA_TRY(cudaDeviceSynchronize());

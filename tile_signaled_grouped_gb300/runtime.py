@@ -238,6 +238,11 @@ class ExpertCombine:
         span, gather span] in ms (-1: none)."""
         return capi.moe_timings(self.plan, 12)
 
+    def producer_spans(self):
+        """[(start_ns, end_ns)] of the producer launches recorded while timing (device
+        clock), oldest first."""
+        return capi.moe_producer_spans(self.plan)
+
     def combine_overlap(self):
         """(share of the combine's bytes landed before the producer's last tile, µs from
         that tile to the last copy, bytes copied) of the last combine recorded."""
