@@ -136,6 +136,7 @@ size_t plan_layout(const Dims& d, size_t* off, size_t* cnt) {
   n[PA_CHUNK_REC] = W * (size_t)d.T * d.k / d.rpc + W * NBM + 1;
   n[PA_CHUNK_T] = 2 * n[PA_CHUNK_REC];
   n[PA_UNIT_TMP] = 4 * W * (size_t)unit_cap(d);
+  n[PA_PAIR_RUN] = W * NMM;
   size_t pos = 0;
   for (int i = 0; i < PA_COUNT; ++i) {
     if (off) off[i] = pos;

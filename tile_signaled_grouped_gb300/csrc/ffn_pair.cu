@@ -213,9 +213,17 @@ __device__ PTask decode_ticket(const PSmem& sm, const ProducerArgs& a, long long
   const int sz1 = u < NU ? unit_at(sm, gub, u + 1) - unit_at(sm, gub, u) : 0;
   int pm;
   if (r < (long long)d.nt1 * sz1) {
+    // A unit's GEMM1 tasks run by run of one expert, hidden-column-major inside a run:
+    // a run's X tiles stay in L2 across its hidden blocks, and consecutive tasks share
+    // a weight tile. Run i's tasks are [nt1 b_i, nt1 b_(i+1)) (b: its first pair's
+    // offset in the unit), so the pair at offset r / nt1 lies in task r's run.
     tk.kind = kPG1;
-    pm = unit_at(sm, gub, u) + (int)(r % sz1);
-    tk.nt = (int)(r / sz1);
+    const int ub = unit_at(sm, gub, u);
+    const int run = __ldg(a.p.a[PA_PAIR_RUN] + ub + (int)(r / d.nt1));
+    const int rs = run & 0xFFFF, rl = run >> 16;
+    const int local = (int)r - d.nt1 * rs;
+    pm = ub + rs + local % rl;
+    tk.nt = local / rl;
   } else {
     r -= (long long)d.nt1 * sz1;
     tk.kind = kPG2;

@@ -94,6 +94,8 @@ enum PlanArray {
   PA_CHUNK_REC,  // [chunks] segment record (consumer order) of every copy chunk
   PA_UNIT_TMP,   // [2][W][2][unit_cap] plan-internal: each unit's first tile in its rank's
                  // phase, then its position in the global tile order
+  PA_PAIR_RUN,   // [pairs] the pair's run of one expert in its unit: first pair's offset in
+                 // the unit + 2^16 * the run's pairs
   PA_COUNT
 };
 

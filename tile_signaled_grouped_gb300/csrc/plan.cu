@@ -560,6 +560,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_order_kernel(DevPlan p) {
     }
     if (tid == 0) p.a[PA_TOTALS][5] = carry_p;
     __syncthreads();
+    // Runs of one expert inside each pair unit (a unit's pairs keep its tiles' expert
+    // runs in order): the producer takes a unit's GEMM1 tasks run by run.
+    const int4* prec = reinterpret_cast<const int4*>(p.a[PA_PAIR]);
+    for (int u = tid; u < NU; u += nt) {
+      const int ub = p.a[PA_PAIR_UNIT_BEGIN][u], ue = p.a[PA_PAIR_UNIT_BEGIN][u + 1];
+      int rs = ub;
+      for (int q = ub; q <= ue; ++q) {
+        if (q == ue || (q > rs && (prec[q].w & 0xFFFF) != (prec[rs].w & 0xFFFF))) {
+          for (int i = rs; i < q; ++i) p.a[PA_PAIR_RUN][i] = (rs - ub) | ((q - rs) << 16);
+          rs = q;
+        }
+      }
+    }
+    __syncthreads();
   }
 
   // 3. Consumer order: segments sorted by the tile of their first band.
