@@ -133,9 +133,9 @@ def source_fingerprint(names) -> str:
 
 def producer_traffic(wl_name: str, reduced: bool, pairs: int):
     """DRAM bytes (read + write) per producer launch, from the committed ncu summary of the
-    A100-like full-size run of the producer in use, while its sources still have the
-    fingerprint recorded there (source_fingerprint); None otherwise (changed kernel, other
-    workload)."""
+    A100-like full-size run of the producer in use, while its sources and the plan build
+    that orders its tiles still have the fingerprint recorded there (source_fingerprint);
+    None otherwise (changed kernel or tile order, other workload)."""
     import re
 
     if wl_name != WORKLOAD or reduced:
@@ -144,7 +144,8 @@ def producer_traffic(wl_name: str, reduced: bool, pairs: int):
                      else ("ffn_producer_a100_like.md", ("ffn.cu",)))
     try:
         text = open(os.path.join(ROOT, "profiles", summary)).read()
-        fp = source_fingerprint(srcs + ("moe_common.cuh",))
+        # plan.cu fixes the order the producer takes its tiles in, so it is part of it.
+        fp = source_fingerprint(srcs + ("moe_common.cuh", "plan.cu"))
     except OSError:
         return None
     m1 = re.search(r"traffic_bytes_per_launch: (\d+)", text)
@@ -332,10 +333,18 @@ def gpu_arm(args, rank, world, local_rank):
     # the previous one drains), so the span rate is beside the rate per step: the
     # executed FLOPs of one step over the whole step time, which can never overlap.
     per_step = flops_exec / (ms_step * 1e-3) / 1e12
-    # The burst peak (cuBLAS timed alone) fits a region of well under a second; over a
-    # seconds-long region the GPU settles at its power cap, which the sustained peak is.
+    # The burst peak (cuBLAS timed alone) fits a region run at full clocks; once the GPU
+    # holds its power cap (a seconds-long region, or a shorter one whose clock samples
+    # show the cap with the SM clock below its maximum) the sustained peak is the one
+    # measured in the same regime.
     region_s = ms_step * args.steps * 1e-3
-    peak, peak_kind = (bf16, "burst") if region_s < 1.0 else (bf16_sus, "sustained")
+    clocks = clk.summary()
+    capped = bool(clocks and clocks.get("window") == "timed region"
+                  and "sw_power_cap" in clocks.get("reasons", [])
+                  and clocks.get("sm_mhz") and clocks.get("sm_max_mhz")
+                  and clocks["sm_mhz"] < clocks["sm_max_mhz"])
+    peak, peak_kind = ((bf16_sus, "sustained") if region_s >= 1.0 or capped
+                       else (bf16, "burst"))
     result = {
         "metric": METRIC,
         "value": job_tokens_per_s(world, W * T, ms_step),
@@ -373,8 +382,10 @@ def gpu_arm(args, rank, world, local_rank):
                      "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "traffic": producer_traffic(wl.name, reduced, args.producer_pairs),
-                     "peak_source": (f"{src} bf16 {peak_kind} (timed region {region_s:.3f} s; "
-                                     "burst below 1 s, sustained above)"),
+                     "peak_source": (f"{src} bf16 {peak_kind} (timed region {region_s:.3f} s"
+                                     + (", clocks held at the power cap" if capped else "")
+                                     + "; burst below 1 s at full clocks, sustained otherwise)"),
+                     "frac_of_burst": achieved / bf16, "frac_of_sustained": achieved / bf16_sus,
                      "flops_per_launch": flops_exec, "launch_ms": prod_avg,
                      "launch_ms_source": ("device clock: the union of the spans (first CTA start "
                                           "to last CTA end) of the producer launches of every "
@@ -388,7 +399,7 @@ def gpu_arm(args, rank, world, local_rank):
         # fused; routed by the gate: gate 1 + plan 4 (the gate set the token bitmaps)
         "gpu_launches": ((9 if wr is None else 8) + (0 if args.consumer_ctas < 0 else 1))
         * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "stages": stages,
         "work": {"rows_executed": rows_exec, "rows_valid": valid_rows,
                  "tflop_executed": flops_exec / 1e12, "tflop_valid": flops_valid / 1e12,
