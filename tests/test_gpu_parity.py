@@ -46,6 +46,9 @@ SMALL = [
     Workload("skew_small", W=4, L=4, topk=1, T=300, d_model=256, d_ff=256, tb_M=256, routing="zipf"),
     Workload("balanced_small", W=4, L=2, topk=2, T=256, d_model=256, d_ff=512, tb_M=128, routing="balanced"),
     Workload("eight_ranks", W=8, L=4, topk=4, T=64, d_model=256, d_ff=256, tb_M=64, routing="gate", mgb=2),
+    # the largest top k the library takes (32), here every expert of every rank
+    Workload("k32_every_expert", W=2, L=16, topk=32, T=24, d_model=128, d_ff=128, tb_M=64,
+             routing="gate"),
 ]
 
 
@@ -189,6 +192,9 @@ ROUTE_SHAPES = [
     Workload("E200", W=8, L=25, topk=8, T=24, d_model=128, d_ff=128, tb_M=64, routing="gate"),
     Workload("E384", W=8, L=48, topk=8, T=16, d_model=128, d_ff=128, tb_M=64, routing="gate"),
     Workload("E1024", W=8, L=128, topk=8, T=16, d_model=128, d_ff=128, tb_M=64, routing="gate"),
+    # the limits together: 256 experts per rank (E = 1024) and top 32
+    Workload("E1024_L256_k32", W=4, L=256, topk=32, T=16, d_model=128, d_ff=128, tb_M=64,
+             routing="gate"),
 ]
 
 

@@ -225,10 +225,22 @@ __device__ PTask decode_ticket(const PSmem& sm, const ProducerArgs& a, long long
     pm = ub + rs + local % rl;
     tk.nt = local / rl;
   } else {
+    // GEMM2 tasks pair-major, except inside a run whose pairs' h fits in 8 MB
+    // (rl * 256 rows * F * 2 bytes): there N-tile-major, so that the run's pairs take
+    // each W_down slice back to back while their h stays in L2.
     r -= (long long)d.nt1 * sz1;
     tk.kind = kPG2;
-    pm = unit_at(sm, gub, u - a.lag) + (int)(r / d.nt2);
-    tk.nt = (int)(r % d.nt2);
+    const int ub = unit_at(sm, gub, u - a.lag);
+    const int run = __ldg(a.p.a[PA_PAIR_RUN] + ub + (int)(r / d.nt2));
+    const int rs = run & 0xFFFF, rl = run >> 16;
+    if ((long long)rl * d.F <= 16384) {
+      const int local = (int)r - d.nt2 * rs;
+      pm = ub + rs + local % rl;
+      tk.nt = local / rl;
+    } else {
+      pm = ub + (int)(r / d.nt2);
+      tk.nt = (int)(r % d.nt2);
+    }
   }
   // One 16-byte record per pair (written by the plan, read-only here).
   const int4 rec = __ldg(reinterpret_cast<const int4*>(a.p.a[PA_PAIR]) + pm);
