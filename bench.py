@@ -390,6 +390,7 @@ def gpu_arm(args, rank, world, local_rank):
                      "launch_ms_source": ("device clock: the union of the spans (first CTA start "
                                           "to last CTA end) of the producer launches of every "
                                           "batch in the timed region, over their number"),
+                     "launches_recorded": len(spans), "launches_timed": args.steps,
                      "span_mean_ms": prod_span_mean,
                      "span_mean_frac": flops_exec / (prod_span_mean * 1e-3) / 1e12 / peak,
                      "per_step_tflops": per_step, "per_step_frac": per_step / peak,

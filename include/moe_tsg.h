@@ -235,7 +235,7 @@ int moe_combine_overlap(moe_plan *plan, double *landed_frac, double *tail_us,
  * the i-th launch's first CTA start and last CTA end on the GPU's global timer
  * (nanoseconds; comparable across the plans of one device, so a caller running
  * several plans in turn can take the union of their launches). At most max_records of
- * the last 64 launches; *count receives how many were written. Synchronises the
+ * the last 1024 launches; *count receives how many were written. Synchronises the
  * device. MOE_ERR_ARG without records. */
 int moe_producer_spans(moe_plan *plan, unsigned long long *start_ns, unsigned long long *end_ns,
                        int max_records, int *count);
@@ -340,7 +340,7 @@ int moe_field(const moe_cfg *cfg, int field, size_t *byte_offset, size_t *count)
  * timing was last enabled (the most recent 64 of them). Synchronises on those
  * events. Order: [0] route (moe_route or moe_gate), [1] plan (all plan kernels and the gather),
  * [2] producer, [3] consumer, [4] scale, [5] gather only. Then, from the device clock,
- * means over the last 64 combines: [6] the producer's execution span (its first CTA's
+ * means over the last 1024 combines: [6] the producer's execution span (its first CTA's
  * start to its last CTA's end; unlike [2] it excludes time spent queued behind other
  * kernels, for example those of another batch in flight, and the launch latency CUDA
  * events include), [7] the span of the scale (moe_scale or moe_scale_gated) after the

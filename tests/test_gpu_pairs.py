@@ -229,22 +229,24 @@ def test_device_clock_spans_of_every_kernel(mode):
 
 def test_producer_spans_one_interval_per_combine():
     """moe_producer_spans: one (start, end) per combine recorded while timing, oldest
-    first, on the device clock; their mean is the producer span of moe_timings slot 6."""
+    first, on the device clock (here more launches than a timed region of a few hundred
+    steps has per batch); their mean is the producer span of moe_timings slot 6."""
     wl = get_workload("tiny")
     inp = P.inputs_for(wl)
     layer = P.run_gpu(wl, inp, mode="fused", canaries=False)
     sp = torch.cuda.Stream()
     layer.set_timing(2)
-    for _ in range(5):
+    n = 150
+    for _ in range(n):
         layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
                       producer=sp)
     torch.cuda.synchronize()
     spans = layer.producer_spans()
     t = layer.timings()
-    assert len(spans) == 5
+    assert len(spans) == n
     assert all(0 < s0 < e0 for s0, e0 in spans)
-    assert all(spans[i][0] >= spans[i - 1][1] for i in range(1, 5))  # one stream: in turn
-    mean_ms = sum(e0 - s0 for s0, e0 in spans) / 5 * 1e-6
+    assert all(spans[i][0] >= spans[i - 1][1] for i in range(1, n))  # one stream: in turn
+    mean_ms = sum(e0 - s0 for s0, e0 in spans) / n * 1e-6
     assert abs(mean_ms - t[6]) <= 1e-3 * t[6] + 1e-6, (mean_ms, t[6])
     layer.set_timing(0)
     with pytest.raises(capi.MoeError, match="ARG"):  # records are off

@@ -178,7 +178,7 @@ def moe_scale_gated(plan, topk_w, recv, out, stream):
           "moe_scale_gated")
 
 
-def moe_producer_spans(plan, max_records=64):
+def moe_producer_spans(plan, max_records=1024):
     """[(start_ns, end_ns)] of the recorded producer launches, oldest first."""
     s = (ctypes.c_ulonglong * max_records)()
     e = (ctypes.c_ulonglong * max_records)()

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <vector>
 #include <climits>
 #include <cstdlib>
 #include <cstring>
@@ -183,6 +184,17 @@ DevPlan dev_plan(const moe_plan* p) {
 unsigned long long* span_record(const moe_plan* p, int slot) {
   return reinterpret_cast<unsigned long long*>(p->plan_ws + p->offsets[PA_SPANS]) +
          (size_t)kSpanWords * (slot % kSpanRing);
+}
+
+// Host copy of the whole ring of device-clock records (kSpanRing x kSpanWords words).
+cudaError_t copy_span_ring(const moe_plan* p, std::vector<unsigned long long>& ring) {
+  try {
+    ring.assign((size_t)kSpanWords * kSpanRing, 0ull);
+  } catch (...) {  // no exception leaves the C ABI
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMemcpy(ring.data(), p->plan_ws + p->offsets[PA_SPANS],
+                    ring.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
 }
 
 struct LaunchShape {
@@ -631,12 +643,12 @@ int moe_producer_spans(moe_plan* p, unsigned long long* start_ns, unsigned long 
       max_records < 0 || !p->spans)
     return MOE_ERR_ARG;
   CUDA_TRY(cudaDeviceSynchronize());
-  unsigned long long ring[kSpanWords * kSpanRing];
-  CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
-                      cudaMemcpyDeviceToHost));
+  std::vector<unsigned long long> ring;
+  CUDA_TRY(copy_span_ring(p, ring));
   const int m = std::min(std::min(p->nspan, kSpanRing), max_records);
   for (int i = 0; i < m; ++i) {  // oldest first
-    const unsigned long long* r = ring + (size_t)kSpanWords * ((p->nspan - m + i) % kSpanRing);
+    const unsigned long long* r =
+        ring.data() + (size_t)kSpanWords * ((p->nspan - m + i) % kSpanRing);
     start_ns[i] = ~r[kSpanProdStart];
     end_ns[i] = r[kSpanProdEnd];
   }
@@ -769,13 +781,13 @@ int moe_timings(moe_plan* p, float* ms, int n) {
   const int m = std::min(p->nspan, kSpanRing);
   if (n > kTSlots && m > 0) {
     CUDA_TRY(cudaDeviceSynchronize());
-    unsigned long long ring[kSpanWords * kSpanRing];
-    CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
-                        cudaMemcpyDeviceToHost));
+    std::vector<unsigned long long> ring;
+    CUDA_TRY(copy_span_ring(p, ring));
     double prod = 0.0, scale = 0.0, beside = 0.0;
     int nscale = 0;
     for (int j = 0; j < m; ++j) {
-      const unsigned long long* r = ring + (size_t)kSpanWords * ((p->nspan - 1 - j) % kSpanRing);
+      const unsigned long long* r =
+          ring.data() + (size_t)kSpanWords * ((p->nspan - 1 - j) % kSpanRing);
       const unsigned long long p0 = ~r[kSpanProdStart], p1 = r[kSpanProdEnd];
       prod += (double)(p1 - p0) * 1e-6;
       if (r[kSpanScaleStart] != 0) {
@@ -796,16 +808,16 @@ int moe_timings(moe_plan* p, float* ms, int n) {
   if (n > kTSlots + 3 && p->spans) {
     const int mg = std::min(p->nspan + 1, kSpanRing);
     CUDA_TRY(cudaDeviceSynchronize());
-    unsigned long long ring[kSpanWords * kSpanRing];
-    CUDA_TRY(cudaMemcpy(ring, p->plan_ws + p->offsets[PA_SPANS], sizeof(ring),
-                        cudaMemcpyDeviceToHost));
+    std::vector<unsigned long long> ring;
+    CUDA_TRY(copy_span_ring(p, ring));
     const int w0[3] = {kSpanGateStart, kSpanConsStart, kSpanGatherStart};
     const int w1[3] = {kSpanGateEnd, kSpanConsEnd, kSpanGatherEnd};
     for (int k = 0; k < 3 && kTSlots + 3 + k < n; ++k) {
       double sum = 0.0;
       int cnt = 0;
       for (int j = 0; j < mg; ++j) {
-        const unsigned long long* r = ring + (size_t)kSpanWords * ((p->nspan - j) % kSpanRing);
+        const unsigned long long* r =
+            ring.data() + (size_t)kSpanWords * ((p->nspan - j) % kSpanRing);
         if (r[w1[k]] != 0 && r[w0[k]] != 0) {
           sum += (double)(r[w1[k]] - ~r[w0[k]]) * 1e-6;
           ++cnt;

@@ -30,7 +30,7 @@ constexpr size_t kConsumerSmemTail = 12 * 1024;  // barriers, counters and recor
 constexpr size_t kConsumerSmem = (size_t)kChunkSlots * kChunkBytes + kConsumerSmemTail;
 constexpr int kSegRec = 8;                   // ints per consumer segment record
 constexpr int kMaxSegChunks = 256;           // copy chunks one segment may have
-constexpr int kSpanRing = 64;                // per-combine device-clock records kept while timing
+constexpr int kSpanRing = 1024;              // per-combine device-clock records kept while timing
 // One record of the span ring: eight u64 device-clock stamps (ns) of one combine.
 enum SpanWord {
   kSpanProdStart = 0,    // ~(first producer CTA start), folded in with atomicMax
