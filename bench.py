@@ -691,8 +691,14 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
     configs = [("cc", c, "after", 1) for c in args.ccta_sweep if c >= -1] + \
               [("scale", args.consumer_ctas, m, n) for n in (1, 2) for m in ("after", "gated")]
     times = {c: [] for c in configs}
+    import random
     for _round in range(4):
-        for cfg in configs:
+        # A slow configuration (one consumer CTA) draws less power, so the one after it
+        # starts at higher clocks: each round takes the configurations in its own
+        # (seeded) order, so that no configuration always follows the same one.
+        order = list(configs)
+        random.Random(_round).shuffle(order)
+        for cfg in order:
             kind, cc, mode, n_fly = cfg
             for lay in pair:
                 lay.set_schedule(cc, wl.mgb)
@@ -720,6 +726,7 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         lay.close()
     del pair
     sweep = {str(c[1]): statistics.median(v) for c, v in times.items() if c[0] == "cc"}
+    sweep_range = {str(c[1]): [min(v), max(v)] for c, v in times.items() if c[0] == "cc"}
     scale_sweep = {f"{c[2]}_x{c[3]}": statistics.median(v) for c, v in times.items()
                    if c[0] == "scale"}
     # The same step captured once into a CUDA graph and replayed (one host launch per step).
@@ -757,8 +764,10 @@ def stage_times(layer, inp, wl, sp, sc, args, iters=12):
         "serial_ms": ser,
         "step_ms_by_consumer_ctas": sweep,
         "step_ms_by_scale_and_batches_in_flight": scale_sweep,
+        "step_ms_by_consumer_ctas_min_max": sweep_range,
         "schedule_sweep_timing": ("whole steps, CUDA events; 4 interleaved rounds of "
-                                  f"{iters} steps per configuration, median"),
+                                  f"{iters} steps per configuration, each round in its own "
+                                  "seeded order, median"),
         "step_ms_graph_replay": graph_ms,
         "producer_alone_tflops": flops / (ser["producer"] * 1e-3) / 1e12,
         "producer_alone_frac_burst": flops / (ser["producer"] * 1e-3) / 1e12 / bf16,
