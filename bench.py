@@ -948,7 +948,7 @@ def main():
                     help="time the gate kernel alone (router scores + softmax + top-k) on the "
                          "workload's tokens; one GPU")
     ap.add_argument("--ccta-sweep", type=lambda v: [int(x) for x in v.split(",") if x],
-                    default=[-1, 0, 4, 8],
+                    default=[-1, 0, 2, 4, 8, 14],
                     help="consumer-CTA counts whose step time is reported (outside the timed "
                          "region); 0 is the serial schedule")
     args = ap.parse_args()
