@@ -192,33 +192,44 @@ class ExpertCombine:
         self.cfg.consumer_ctas, self.cfg.mgb = consumer_ctas, mgb
 
     def tune(self, x, w_gate, w_up, w_down, logits, forced_ids=None, producer=None,
-             consumer=None, candidates=((-1, 1), (0, 1), (4, 1), (8, 1), (4, 2)), steps=6):
+             consumer=None, candidates=((-1, 1), (0, 1), (4, 1), (8, 1), (14, 1), (4, 2)),
+             steps=6, rounds=3):
         """Adaptive schedule: times whole steps on these inputs for each (consumer_ctas,
         mgb) candidate and keeps the fastest. Returns (consumer_ctas, mgb, {candidate:
-        ms per step}). Candidates the shape does not support are skipped."""
+        median ms per step}). Candidates the shape does not support are skipped. The
+        candidates take turns over `rounds` rounds, each in a rotated order, and each
+        keeps its median: the GPU's clocks follow its power draw, so a candidate timed
+        right after a slow (low-power) one would otherwise start at higher clocks."""
         sp = producer if producer is not None else torch.cuda.Stream(device=self.device)
         sc = consumer if consumer is not None else torch.cuda.Stream(device=self.device,
                                                                      priority=-1)
         keep = (self.cfg.consumer_ctas, self.cfg.mgb)
-        times = {}
-        for cc, mgb in candidates:
+        usable = []
+        for cand in candidates:
             try:
-                self.set_schedule(cc, mgb)
+                self.set_schedule(*cand)
             except capi.MoeError:
                 continue
-            run = lambda: self.forward(x, w_gate, w_up, w_down, logits, forced_ids, sp, sc)
-            run()
-            run()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(sp)
-            for _ in range(steps):
+            usable.append(tuple(cand))
+        samples = {c: [] for c in usable}
+        run = lambda: self.forward(x, w_gate, w_up, w_down, logits, forced_ids, sp, sc)
+        for r in range(max(1, rounds)):
+            k = r % len(usable) if usable else 0
+            for cc, mgb in usable[k:] + usable[:k]:
+                self.set_schedule(cc, mgb)
                 run()
-            e1.record(sp)
-            e1.synchronize()
-            if self.status() != (0, 0):
-                raise capi.MoeError(f"device status {self.status()} while tuning {cc, mgb}")
-            times[(cc, mgb)] = e0.elapsed_time(e1) / steps
+                run()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(sp)
+                for _ in range(steps):
+                    run()
+                e1.record(sp)
+                e1.synchronize()
+                if self.status() != (0, 0):
+                    raise capi.MoeError(f"device status {self.status()} while tuning {cc, mgb}")
+                samples[(cc, mgb)].append(e0.elapsed_time(e1) / steps)
+        times = {c: sorted(v)[len(v) // 2] for c, v in samples.items()}
         best = min(times, key=times.get) if times else keep
         self.set_schedule(*best)
         return best[0], best[1], times
