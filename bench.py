@@ -170,6 +170,21 @@ def producer_launch_ms(spans) -> float:
     return busy / len(spans) * 1e-6
 
 
+def pick_bf16_peak(region_s: float, clocks, burst: float, sustained: float):
+    """(peak, "burst" | "sustained", capped): the measured bf16 peak whose conditions match
+    the timed region's. The burst figure (cuBLAS timed alone) fits a region run at full
+    clocks; once the GPU holds its power cap (a region of a second or more, or a shorter
+    one whose clock samples show sw_power_cap with the SM clock below its maximum) the
+    sustained figure, measured in the same regime, does."""
+    capped = bool(clocks and clocks.get("window") == "timed region"
+                  and "sw_power_cap" in clocks.get("reasons", [])
+                  and clocks.get("sm_mhz") and clocks.get("sm_max_mhz")
+                  and clocks["sm_mhz"] < clocks["sm_max_mhz"])
+    if region_s >= 1.0 or capped:
+        return sustained, "sustained", capped
+    return burst, "burst", capped
+
+
 def max_over_ranks(v: float, device="cpu") -> float:
     """Largest value over the ranks of the default process group (v itself alone)."""
     import torch
@@ -333,18 +348,9 @@ def gpu_arm(args, rank, world, local_rank):
     # the previous one drains), so the span rate is beside the rate per step: the
     # executed FLOPs of one step over the whole step time, which can never overlap.
     per_step = flops_exec / (ms_step * 1e-3) / 1e12
-    # The burst peak (cuBLAS timed alone) fits a region run at full clocks; once the GPU
-    # holds its power cap (a seconds-long region, or a shorter one whose clock samples
-    # show the cap with the SM clock below its maximum) the sustained peak is the one
-    # measured in the same regime.
     region_s = ms_step * args.steps * 1e-3
     clocks = clk.summary()
-    capped = bool(clocks and clocks.get("window") == "timed region"
-                  and "sw_power_cap" in clocks.get("reasons", [])
-                  and clocks.get("sm_mhz") and clocks.get("sm_max_mhz")
-                  and clocks["sm_mhz"] < clocks["sm_max_mhz"])
-    peak, peak_kind = ((bf16_sus, "sustained") if region_s >= 1.0 or capped
-                       else (bf16, "burst"))
+    peak, peak_kind, capped = pick_bf16_peak(region_s, clocks, bf16, bf16_sus)
     result = {
         "metric": METRIC,
         "value": job_tokens_per_s(world, W * T, ms_step),

@@ -131,3 +131,17 @@ def test_source_fingerprint_ignores_comments(tmp_path, monkeypatch):
     assert bench.source_fingerprint(("k.cu",)) == fp
     (csrc / "k.cu").write_text("int a = 1;\nint b = 3;\n")
     assert bench.source_fingerprint(("k.cu",)) != fp
+
+
+def test_peak_follows_the_clock_regime_of_the_timed_region():
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "window": "timed region"}
+    capped = {"sm_mhz": 1758.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+              "window": "timed region"}
+    at_max = dict(capped, sm_mhz=2070.0)  # the cap flagged, the clock still at its maximum
+    outside = dict(capped, window="whole sampler run (none inside the region)")
+    assert bench.pick_bf16_peak(0.035, full, 1945.0, 1707.2) == (1945.0, "burst", False)
+    assert bench.pick_bf16_peak(0.4, capped, 1945.0, 1707.2) == (1707.2, "sustained", True)
+    assert bench.pick_bf16_peak(0.4, at_max, 1945.0, 1707.2) == (1945.0, "burst", False)
+    assert bench.pick_bf16_peak(0.4, outside, 1945.0, 1707.2) == (1945.0, "burst", False)
+    assert bench.pick_bf16_peak(3.0, full, 1945.0, 1707.2) == (1707.2, "sustained", False)
+    assert bench.pick_bf16_peak(0.035, None, 1945.0, 1707.2) == (1945.0, "burst", False)
