@@ -213,6 +213,24 @@ def test_worked_example_figure2():
     assert p.recv_rows.tolist() == g["recv_rows"]
 
 
+def test_rule_ii_tie_keeps_the_lower_local_index_first():
+    """Rule (ii) with equal remote loads (the pages leave the order of a tie open; the
+    reading taken is the lower local index first, as in the balanced A100-like layer).
+    Hand-derived: W = 2, L = 2, tb_M = 2; every rank sends token 0 to experts 0 and 2
+    and token 1 to experts 1 and 3. On rank 0, expert 0 holds one remote row (rank 1's
+    token 0) padded to a 2-row band, then its one local row: bands 0 (remote, to rank
+    1) and 1 (local); expert 1 likewise at rows 4..7: bands 2 and 3. Both experts have
+    one remote band, so S = [0, 2, 1, 3]: both remote bands, expert 0's first, then the
+    local bands in local-index order."""
+    ids = np.array([[[0, 2], [1, 3]], [[0, 2], [1, 3]]])
+    p = O.build_plan(ids, 2, 2, 2, 1)
+    for r in range(2):
+        assert p.nrb[2 * r:2 * r + 2].tolist() == [1, 1]
+        assert p.band_dst[r].tolist() == [1 - r, r, 1 - r, r]
+        assert p.S[r].tolist() == [0, 2, 1, 3]
+        assert p.n_remote[r] == 2
+
+
 def test_padding_bound_closed_forms():
     g = _load("padding_bounds.json")
     for c in g["cases"]:
