@@ -99,6 +99,13 @@ struct PairCfg {
 static_assert(PairCfg<false>::kSmem <= 227 * 1024, "pair producer shared memory");
 static_assert(PairCfg<true>::kSmem <= 227 * 1024, "fused pair producer shared memory");
 
+// One 32-byte store (a whole L2 sector); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // --- cluster and cta_group::2 forms ------------------------------------------
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
@@ -513,6 +520,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
       const int grow = tk.row0 + r;
       const bool valid = tk.own >= 0 && grow < rows_lim;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPAccCols);
+      // Row offsets and column offsets are multiples of 64 bytes (D, F multiples of 128), so
+      // the output's base alignment decides whether 32-byte stores are aligned.
+      const bool v8ok = ((reinterpret_cast<uintptr_t>(tk.kind == kPG1 ? (const void*)a.h[tk.o]
+                                                                     : (const void*)a.y[tk.o])) &
+                         31) == 0;
       if (tk.kind == kPG1) {
         uint4* out = reinterpret_cast<uint4*>(a.h[tk.o] + (size_t)grow * d.F + tk.nt * kN1);
 #pragma unroll 1
@@ -530,7 +542,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
             const float a1 = g1v / (1.0f + __expf(-g1v)) * u1;
             packed[i] = pack_bf16x2(a0, a1);
           }
-          if (valid) {
+          if (valid && v8ok) {
+            st_global_v8(out + c * 4, packed);
+            st_global_v8(out + c * 4 + 2, packed + 8);
+          } else if (valid) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               out[c * 4 + i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
@@ -552,7 +567,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
             pv[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
             pw[i] = pack_bf16x2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
           }
-          if (valid) {
+          if (valid && v8ok) {
+            st_global_v8(out + c * 4, pv);
+            st_global_v8(out + c * 4 + 2, pv + 8);
+            st_global_v8(out + c * 4 + 4, pw);
+            st_global_v8(out + c * 4 + 6, pw + 8);
+          } else if (valid) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               out[c * 4 + i] = make_uint4(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
