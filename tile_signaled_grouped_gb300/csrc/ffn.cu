@@ -326,6 +326,12 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
       const int grow = tk.row0 + r;
       const bool valid = grow < rows_lim;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kAccCols);
+      // Each thread writes its row's 64-byte runs as two 32-byte stores (whole L2 sectors):
+      // row and column offsets are multiples of 64 bytes (D, F multiples of 128), so the
+      // output's base alignment decides; an unaligned base keeps 16-byte stores.
+      const bool v8ok = ((reinterpret_cast<uintptr_t>(tk.kind == kG1 ? (const void*)a.h[tk.o]
+                                                                    : (const void*)a.y[tk.o])) &
+                         31) == 0;
       if (tk.kind == kG1) {
         uint4* out = reinterpret_cast<uint4*>(a.h[tk.o] + (size_t)grow * d.F + tk.nt * kN1);
 #pragma unroll 1
@@ -343,7 +349,10 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
             const float a1 = g1v / (1.0f + __expf(-g1v)) * u1;
             packed[i] = pack_bf16x2(a0, a1);
           }
-          if (valid) {
+          if (valid && v8ok) {
+            st_global_v8(out + c * 4, packed);
+            st_global_v8(out + c * 4 + 2, packed + 8);
+          } else if (valid) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               out[c * 4 + i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
@@ -361,7 +370,10 @@ __global__ void __launch_bounds__(kProducerThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          if (valid) {
+          if (valid && v8ok) {
+            st_global_v8(out + c * 4, packed);
+            st_global_v8(out + c * 4 + 2, packed + 8);
+          } else if (valid) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               out[c * 4 + i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],

@@ -99,13 +99,6 @@ struct PairCfg {
 static_assert(PairCfg<false>::kSmem <= 227 * 1024, "pair producer shared memory");
 static_assert(PairCfg<true>::kSmem <= 227 * 1024, "fused pair producer shared memory");
 
-// One 32-byte store (a whole L2 sector); the address must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-
 // --- cluster and cta_group::2 forms ------------------------------------------
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
