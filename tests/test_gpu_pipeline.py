@@ -161,3 +161,28 @@ def test_captured_graph_replays_exactly(cctas, scale):
         assert layer.status() == (0, 0)
         for got, ref in zip(layer.out, want[i]):
             assert torch.equal(got, ref), f"replay with input set {i}"
+
+
+def test_new_layer_runs_at_once_on_a_side_stream():
+    """A layer used on a side stream right after construction: its zero-filled plan
+    workspace and receive buffers are ready before the first combine (the fills run on
+    the current stream, and torch's side streams do not wait for it). Layers are
+    created where the previous one's memory was just freed, the case that raced."""
+    wl = get_workload("qwen3_235b_like")
+    inp = P.inputs_for(wl)
+    torch.cuda.synchronize()
+    first = None
+    for _ in range(4):
+        layer = ExpertCombine(wl.W, wl.L, wl.topk, wl.T, wl.d_model, wl.d_ff, wl.tb_M, wl.mgb)
+        sp = torch.cuda.Stream()
+        layer.forward(inp.x, inp.w_gate, inp.w_up, inp.w_down, inp.logits, inp.forced_ids,
+                      producer=sp)
+        torch.cuda.synchronize()
+        assert layer.status() == (0, 0)
+        out = [t.clone() for t in layer.out]
+        if first is None:
+            first = out
+        assert all(torch.equal(a, b) for a, b in zip(first, out))
+        layer.close()
+        del layer
+        torch.cuda.empty_cache()

@@ -58,6 +58,11 @@ class ExpertCombine:
         with torch.cuda.device(dev):
             self.plan = capi.moe_plan_create(self.cfg, self.plan_ws.data_ptr(), plan_bytes,
                                              [t.data_ptr() for t in self.rank_ws], rank_bytes)
+        # The zero fills above ran on the current stream, and the layer's kernels run on
+        # the caller's streams, which torch creates non-blocking: without this wait a
+        # first combine could start while the plan workspace (counters, flags, status)
+        # or a receive buffer is still being zeroed.
+        torch.cuda.synchronize(dev)
 
     def close(self):
         if getattr(self, "plan", None):
