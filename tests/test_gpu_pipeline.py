@@ -169,7 +169,7 @@ def test_new_layer_runs_at_once_on_a_side_stream():
     the current stream, and torch's side streams do not wait for it). Layers are
     created where the previous one's memory was just freed, the case that raced."""
     wl = get_workload("qwen3_235b_like")
-    inp = P.inputs_for(wl)
+    inp = make_inputs(wl, device="cuda")
     torch.cuda.synchronize()
     first = None
     for _ in range(4):
