@@ -254,7 +254,11 @@ __device__ PTask decode_ticket(const PSmem& sm, const ProducerArgs& a, long long
 }
 
 template <bool FUSED>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThreads, 1)
+// At most 104 registers a thread (384 threads: 39,936 of the SM's 65,536), so that a
+// 256-thread CTA of up to 96 registers (the scale, the gather, the plan kernels of the
+// other batch in flight) fits beside a producer CTA; without the cap the compiler took
+// 118, and the scale then waited for the whole next producer to finish.
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(104)
     ffn_pair_kernel(const __grid_constant__ ProducerArgs a) {
   constexpr int kPStages = PairCfg<FUSED>::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -531,8 +535,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<FUSED>::kThr
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(g[2 * i]), g1v = __uint_as_float(g[2 * i + 1]);
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            const float a0 = g0 / (1.0f + __expf(-g0)) * u0;
-            const float a1 = g1v / (1.0f + __expf(-g1v)) * u1;
+            const float a0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+            const float a1 = __fdividef(g1v, 1.0f + __expf(-g1v)) * u1;
             packed[i] = pack_bf16x2(a0, a1);
           }
           if (valid && v8ok) {
