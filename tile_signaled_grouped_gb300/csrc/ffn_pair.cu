@@ -535,6 +535,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(104)
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(g[2 * i]), g1v = __uint_as_float(g[2 * i + 1]);
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            // SiLU(g) u = g / (1 + e^-g) u. The fast division (an approximate reciprocal)
+            // is far cheaper than the IEEE one, which made this loop the epilogue's cost,
+            // and h is rounded to bf16 right after.
             const float a0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
             const float a1 = __fdividef(g1v, 1.0f + __expf(-g1v)) * u1;
             packed[i] = pack_bf16x2(a0, a1);
